@@ -1,0 +1,82 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the benchmark.
+
+This module only draws random numbers in the shapes and distributions of the
+workloads the pages measure ("[AMD] Small-M FP8 block-scale GEMM with fused
+activation quant for gfx950 (Qwen3.5)", sections "Modifications" and "Kernel
+microbenchmarks": the projection shapes 5120x4096, 4608x4096, 4096x2048 at
+1..32 tokens).  It holds none of the method's arithmetic: no quantisation, no
+scales, no GEMM.  Both the CUDA library's callers and the CPU oracle's callers
+take their inputs from here, so both sides see identical bytes.
+
+Recipes:
+  x  -- bf16 [M, K]: fp32 N(0, 1), optionally with each entry independently
+        chosen with probability 1% and multiplied by 20 (outliers), then
+        rounded to bf16 (nearest even).
+  W  -- fp32 [N, K]: N(0, 0.02).
+Seeds: ``seed = 1000 * workload + copy`` by convention of the callers.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+OUTLIER_FRACTION = 0.01
+OUTLIER_SCALE = 20.0
+WEIGHT_STD = 0.02
+
+
+def _rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(int(seed)))
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def x_bf16(M: int, K: int, seed: int, outliers: bool = True) -> np.ndarray:
+    """Activations as bf16 bit patterns, uint16 [M, K]."""
+    rng = _rng(seed)
+    v = rng.standard_normal((M, K), dtype=np.float32)
+    if outliers:
+        pick = rng.random((M, K)) < OUTLIER_FRACTION
+        v = np.where(pick, v * np.float32(OUTLIER_SCALE), v).astype(np.float32)
+    return f32_to_bf16_bits(v)
+
+
+def w_f32(N: int, K: int, seed: int) -> np.ndarray:
+    """Weights before block quantisation, float32 [N, K] ~ N(0, 0.02)."""
+    rng = _rng(seed)
+    return (rng.standard_normal((N, K), dtype=np.float32) * np.float32(WEIGHT_STD)).astype(
+        np.float32)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Device-side draws for the benchmark's large rotated weight sets.  These use
+# torch's CUDA generator: the same recipe, a different stream of numbers, so
+# they never stand in for an oracle comparison.
+# ---------------------------------------------------------------------------
+
+def x_bf16_torch(M: int, K: int, seed: int, device, outliers: bool = True):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    v = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
+    if outliers:
+        pick = torch.rand((M, K), generator=g, device=device) < OUTLIER_FRACTION
+        v = torch.where(pick, v * OUTLIER_SCALE, v)
+    return v.to(torch.bfloat16)
+
+
+def w_f32_torch(N: int, K: int, seed: int, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * WEIGHT_STD
