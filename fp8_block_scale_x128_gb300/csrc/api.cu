@@ -1,0 +1,195 @@
+// C ABI of the fp8bs library (declared in include/fp8bs.h).
+//
+// Every entry point checks its arguments on the host first, in this order:
+// null pointers and the scale kind (FP8BS_ERR_ARG), shapes (FP8BS_ERR_SHAPE),
+// strides and alignment (FP8BS_ERR_ALIGN), buffer sizes (FP8BS_ERR_WORKSPACE).
+// Nothing is enqueued when a check fails, and no check touches the GPU, so the
+// checks run on machines without one.  The support rules follow "[AMD] Small-M
+// FP8 block-scale GEMM with fused activation quant for gfx950 (Qwen3.5)",
+// "Modifications" (bf16 input with 16-byte aligned rows, a contiguous
+// [N/128, K/128] weight scale, M <= 32); a mismatching scale kind is refused
+// rather than reinterpreted, as "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM
+// for dense 128x128 fp8 linears (6/8)", "Modifications" requires.
+#include <cuda_runtime.h>
+
+#include "internal.cuh"
+
+namespace {
+
+using namespace fp8bs;
+
+constexpr int64_t kMaxDim = int64_t(1) << 24;  // N, K bound (keeps every index in range)
+constexpr long long kDefaultTimeoutCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool kind_ok(int kind) { return kind == FP8BS_SCALE_F32 || kind == FP8BS_SCALE_UE8M0; }
+
+bool nk_ok(int64_t N, int64_t K) {
+    return N >= kTile && K >= kTile && N % kTile == 0 && K % kTile == 0 && N <= kMaxDim && K <= kMaxDim;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int current_sm_count(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
+    static int cache[64] = {0};
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return FP8BS_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return FP8BS_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return FP8BS_OK;
+}
+
+size_t workspace_bytes_for(int64_t N, int64_t K, int sm_count) {
+    const size_t g = static_cast<size_t>(fused_max_grid(N, K, sm_count));
+    return ws_partials_offset() + g * 2 * kPartialSlotFloats * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8bs_status_string(int status) {
+    switch (status) {
+        case FP8BS_OK: return "ok";
+        case FP8BS_ERR_ARG: return "invalid argument (null pointer, scale kind or stride)";
+        case FP8BS_ERR_SHAPE: return "unsupported shape (M, N or K)";
+        case FP8BS_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+        case FP8BS_ERR_SCALE_KIND: return "packed weight has another scale kind or shape";
+        case FP8BS_ERR_WORKSPACE: return "workspace or packed buffer too small or misaligned";
+        case FP8BS_ERR_CUDA: return "CUDA runtime error";
+        case FP8BS_ERR_TIMEOUT: return "device wait timed out";
+        case FP8BS_ERR_DEVICE: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+int fp8bs_version(void) { return (1 << 16) | 0; }
+
+int fp8bs_encode_e4m3(const float* v, int64_t n, uint8_t* codes, void* stream) {
+    if (n < 0 || n % 4 != 0) return FP8BS_ERR_SHAPE;
+    if (n == 0) return FP8BS_OK;
+    if (!v || !codes) return FP8BS_ERR_ARG;
+    if (!aligned(v, 16) || !aligned(codes, 4)) return FP8BS_ERR_ALIGN;
+    return status_of(launch_encode_e4m3(v, n, codes, as_stream(stream)));
+}
+
+int fp8bs_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int scale_kind, uint8_t* xq,
+                void* xs, void* stream) {
+    if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;
+    if (M < 0 || K < kTile || K % kTile != 0 || K > kMaxDim || M > kMaxDim) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !xq || !xs) return FP8BS_ERR_ARG;
+    if (ldx < K) return FP8BS_ERR_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(xq, 8) ||
+        (scale_kind == FP8BS_SCALE_F32 && !aligned(xs, 4)))
+        return FP8BS_ERR_ALIGN;
+    return status_of(launch_quant(x, M, K, ldx, scale_kind, xq, xs, as_stream(stream)));
+}
+
+int fp8bs_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int scale_kind, uint8_t* wq,
+                       void* ws, void* stream) {
+    if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;
+    if (!nk_ok(N, K)) return FP8BS_ERR_SHAPE;
+    if (!w || !wq || !ws) return FP8BS_ERR_ARG;
+    if (ldw < K) return FP8BS_ERR_ARG;
+    if (!aligned(w, 16) || ldw % 4 != 0 || !aligned(wq, 16) ||
+        (scale_kind == FP8BS_SCALE_F32 && !aligned(ws, 4)))
+        return FP8BS_ERR_ALIGN;
+    return status_of(launch_quant_weight(w, N, K, ldw, scale_kind, wq, ws, as_stream(stream)));
+}
+
+size_t fp8bs_packed_weight_bytes(int64_t N, int64_t K, int scale_kind) {
+    if (!kind_ok(scale_kind) || !nk_ok(N, K)) return 0;
+    const size_t tiles = static_cast<size_t>(N / kTile) * static_cast<size_t>(K / kTile);
+    const size_t scale_bytes = tiles * (scale_kind == FP8BS_SCALE_F32 ? 4 : 1);
+    return round_up(packed_scales_offset(N, K) + scale_bytes, 256);
+}
+
+int fp8bs_prepack_weight(const uint8_t* wq, int64_t ldw, const void* ws, int64_t N, int64_t K,
+                         int scale_kind, void* packed, size_t packed_bytes, void* stream) {
+    if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;
+    if (!nk_ok(N, K)) return FP8BS_ERR_SHAPE;
+    if (!wq || !ws || !packed) return FP8BS_ERR_ARG;
+    if (ldw < K) return FP8BS_ERR_ARG;
+    if (!aligned(wq, 16) || ldw % 16 != 0 || !aligned(packed, 256) ||
+        (scale_kind == FP8BS_SCALE_F32 && !aligned(ws, 4)))
+        return FP8BS_ERR_ALIGN;
+    if (packed_bytes < fp8bs_packed_weight_bytes(N, K, scale_kind)) return FP8BS_ERR_WORKSPACE;
+    return status_of(launch_prepack(wq, ldw, ws, N, K, scale_kind, packed, as_stream(stream)));
+}
+
+size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count) {
+    if (!nk_ok(N, K) || N > kMaxFusedN) return 0;
+    if (sm_count <= 0 && current_sm_count(&sm_count) != FP8BS_OK) return 0;
+    return workspace_bytes_for(N, K, sm_count);
+}
+
+int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace) return FP8BS_ERR_ARG;
+    if (!aligned(workspace, 256)) return FP8BS_ERR_ALIGN;
+    if (workspace_bytes < kWsErrorBytes) return FP8BS_ERR_WORKSPACE;
+    return status_of(cudaMemsetAsync(workspace, 0, workspace_bytes, as_stream(stream)));
+}
+
+int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* packed, size_t packed_bytes,
+                     int64_t N, int64_t K, int scale_kind, uint16_t* y, int64_t ldy, void* workspace,
+                     size_t workspace_bytes, uint8_t* xq_out, void* xs_out, void* stream) {
+    if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;
+    if (M < 0 || M > FP8BS_MAX_M || !nk_ok(N, K) || N > kMaxFusedN) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !packed || !y || !workspace) return FP8BS_ERR_ARG;
+    if (ldx < K || ldy < N) return FP8BS_ERR_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(y, 16) || ldy % 8 != 0 || !aligned(packed, 256) ||
+        !aligned(workspace, 256) || (xq_out && !aligned(xq_out, 16)) ||
+        (xs_out && scale_kind == FP8BS_SCALE_F32 && !aligned(xs_out, 4)))
+        return FP8BS_ERR_ALIGN;
+    if (packed_bytes < fp8bs_packed_weight_bytes(N, K, scale_kind)) return FP8BS_ERR_WORKSPACE;
+    int sm = 0;
+    const int rc = current_sm_count(&sm);
+    if (rc != FP8BS_OK) return rc;
+    if (workspace_bytes < workspace_bytes_for(N, K, sm)) return FP8BS_ERR_WORKSPACE;
+    FusedArgs a;
+    a.x = x;
+    a.ldx = ldx;
+    a.packed = static_cast<const uint8_t*>(packed);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.kind = scale_kind;
+    a.y = y;
+    a.ldy = ldy;
+    a.workspace = static_cast<uint8_t*>(workspace);
+    a.xq_out = xq_out;
+    a.xs_out = xs_out;
+    a.sm_count = sm;
+    a.timeout_cycles = kDefaultTimeoutCycles;
+    return status_of(launch_fused(a, as_stream(stream)));
+}
+
+int fp8bs_check_error(void* workspace, void* stream) {
+    if (!workspace) return FP8BS_ERR_ARG;
+    if (!aligned(workspace, 256)) return FP8BS_ERR_ALIGN;
+    cudaStream_t s = as_stream(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FP8BS_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FP8BS_ERR_CUDA;
+    if (word != 0) {
+        const uint32_t zero = 0;
+        if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8BS_ERR_CUDA;
+        return -static_cast<int>(word);
+    }
+    return FP8BS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+/*
+ * fp8bs -- small-M W8A8 FP8 block-scale linear for NVIDIA GB300 (sm_103a).
+ *
+ *   Y[M,N] = bf16( sum_kb ( sum_{k in kb} xq[m,k] * wq[n,k] ) * xs[m,kb] * ws[n/128,kb] )
+ *
+ * with the bf16 -> e4m3fn activation quantisation in 1x128 groups fused into
+ * the same launch, and an optional power-of-two (ue8m0 / e8m0) scale variant.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "[AMD] Small-M FP8 block-scale GEMM with fused activation quant for
+ *        gfx950 (Qwen3.5)", "Motivation" and "Modifications": one launch per
+ *        linear for M <= 32; per-1x128-group activation quant from the row amax,
+ *        bit-exact scales and fp8 bytes; the fp8 weight streamed once; one MMA
+ *        per 128-wide K block followed by x_scale * w_scale in fp32; a cross-wave
+ *        reduction to a bf16 output; a [N/128, K/128] fp32 weight scale; the
+ *        support rules (bf16 input, 16-byte aligned rows, contiguous scales, no
+ *        bias, no input scale).
+ *   [P2] "[AMD] gfx950 small-batch MoE: expert-count gate for the small sort and
+ *        FP8 block-scale small-M kernel", "Modifications": float8_e4m3fn weights
+ *        with a 128x128 fp32 block scale applied to each partial sum.
+ *   [P4] "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense 128x128 fp8
+ *        linears (6/8)", "Motivation" and "Modifications": power-of-two 128x128
+ *        weight scales kept as one e8m0 byte per block; ue8m0 per-1x128
+ *        activation scales; an e8m0 operand must never be read as fp32.
+ *
+ * Conventions for every entry point:
+ *   - Data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory, keeps no pointer after a call returns and never
+ *     synchronises, except fp8bs_check_error (documented there).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it; results are ready when it reaches them.
+ *   - Return value: FP8BS_OK (0) or a negative fp8bs_status.  Argument faults
+ *     are detected on the host, return at once and enqueue nothing.  Faults only
+ *     the device can see (a packed weight of another shape or scale kind, a
+ *     bounded wait that expired) are recorded in the workspace error word and
+ *     reported by fp8bs_check_error.
+ *   - Layouts are row-major.  bf16 values travel as uint16_t bit patterns and
+ *     e4m3fn codes / e8m0 scale bytes as uint8_t.
+ *   - e4m3fn: OCP FP8 E4M3 (bias 7, no infinities, largest finite 448).  Codes
+ *     are round-to-nearest-even of x / scale, saturated to +-448, never NaN.
+ *   - Scale kinds: FP8BS_SCALE_F32 stores fp32 scales; FP8BS_SCALE_UE8M0 stores
+ *     one e8m0 byte b per scale, meaning 2^(b - 127).  The kind is always an
+ *     explicit argument and is never inferred from the bytes [P4].
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_SCALE_F32 = 0,   /* fp32 scales: activation scale = amax / 448 */
+    FP8BS_SCALE_UE8M0 = 1, /* e8m0 bytes: activation scale = 2^ceil(log2(amax / 448)) */
+} fp8bs_scale_kind;
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_ARG = -1,        /* null pointer, unknown scale kind, bad stride */
+    FP8BS_ERR_SHAPE = -2,      /* M, N or K outside the supported range */
+    FP8BS_ERR_ALIGN = -3,      /* a pointer or row stride is not 16-byte aligned */
+    FP8BS_ERR_SCALE_KIND = -4, /* packed weight holds another scale kind or shape */
+    FP8BS_ERR_WORKSPACE = -5,  /* workspace or packed buffer too small / misaligned */
+    FP8BS_ERR_CUDA = -6,       /* a CUDA runtime call failed (launch, copy, attribute) */
+    FP8BS_ERR_TIMEOUT = -7,    /* device: a bounded wait expired; outputs are invalid */
+    FP8BS_ERR_DEVICE = -8,     /* device: another device-side check failed */
+} fp8bs_status;
+
+/* Largest token count of the fused GEMM ([P1] "Motivation": one launch for
+ * M <= 32; larger inputs keep the library path). */
+#define FP8BS_MAX_M 32
+
+/* Text for a status code.  Never NULL; static storage. */
+const char* fp8bs_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int fp8bs_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Activation quantisation ([P1] "Modifications", the first of the two old   */
+/* launches; [P4] "Modifications", ue8m0 per-1x128 quant)                   */
+/* ------------------------------------------------------------------------ */
+
+/* Quantise bf16 activations in 1x128 groups along K.
+ *   x   : bf16 [M, K], row stride ldx elements.  x and ldx*2 bytes must be
+ *         16-byte aligned.
+ *   M   : rows, M >= 0 (0 enqueues nothing and returns FP8BS_OK).
+ *   K   : multiple of 128, K >= 128.
+ *   xq  : e4m3fn codes [M, K], row stride K (4-byte aligned).
+ *   xs  : [M, K/128]: fp32 (kind F32, 4-byte aligned) or e8m0 bytes (UE8M0).
+ * Per group: amax = max |x| (fp32); F32: s = amax / 448 (IEEE fp32 division);
+ * UE8M0: s = smallest power of two >= fp32(amax / 448), exponent clamped to
+ * [-127, 127].  Codes = e4m3fn RNE-saturated of x / s (IEEE fp32 division).
+ * A group with amax == 0 gets s = 0 (F32) or byte 0 (UE8M0) and signed zeros.
+ * Errors: FP8BS_ERR_ARG, FP8BS_ERR_SHAPE, FP8BS_ERR_ALIGN, FP8BS_ERR_CUDA. */
+int fp8bs_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int scale_kind,
+                uint8_t* xq, void* xs, void* stream);
+
+/* Quantise an fp32 weight in 128x128 blocks (the offline producer of the
+ * [N/128, K/128] weight scale of [P1] "Modifications"; with UE8M0 each block
+ * scale is rounded up to a power of two as in [P4] "Motivation").
+ *   w   : fp32 [N, K], row stride ldw elements; w and ldw*4 16-byte aligned.
+ *   N,K : multiples of 128, >= 128.
+ *   wq  : e4m3fn codes [N, K], row stride K (16-byte aligned).
+ *   ws  : [N/128, K/128] fp32 or e8m0 bytes.
+ * Same rounding rules as fp8bs_quant, over each 128x128 block. */
+int fp8bs_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int scale_kind,
+                       uint8_t* wq, void* ws, void* stream);
+
+/* Encode fp32 values to e4m3fn codes with the rounding every kernel of this
+ * library uses (round to nearest even, finite magnitudes >= 448 saturate to
+ * +-448, NaN in gives NaN out).  A diagnostic of the encoder behind the quant
+ * entry points ([P2] "Modifications" names float8_e4m3fn).
+ *   v     : fp32 [n], 16-byte aligned.
+ *   codes : uint8 [n], 4-byte aligned.
+ *   n     : >= 0, a multiple of 4 (0 enqueues nothing). */
+int fp8bs_encode_e4m3(const float* v, int64_t n, uint8_t* codes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weight prepack (GB300 layout; replaces the (16,16) pre-shuffle of [P1]    */
+/* "Modifications", which is specific to the gfx950 MFMA operand order)     */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of a packed weight: a 256-byte header, N/128 * K/128 tiles of 16384
+ * bytes, then the scales (4 or 1 byte per tile), rounded up to 256 bytes.
+ * Returns 0 for an invalid shape or kind. */
+size_t fp8bs_packed_weight_bytes(int64_t N, int64_t K, int scale_kind);
+
+/* Pack an e4m3fn weight and its block scales for fp8bs_gemm_fused.
+ *   wq     : e4m3fn codes [N, K], row stride ldw bytes (wq and ldw 16-byte aligned).
+ *   ws     : [N/128, K/128] contiguous: fp32 for F32, e8m0 bytes for UE8M0.
+ *   packed : output, >= fp8bs_packed_weight_bytes(N, K, scale_kind) bytes,
+ *            256-byte aligned.  Layout: header {magic, version, N, K, kind};
+ *            tile (nt, kb) at 256 + (nt * K/128 + kb) * 16384 holding rows
+ *            nt*128 .. +127 and columns kb*128 .. +127 of wq in the shared-
+ *            memory operand image of a K-major, 128-byte-swizzled MMA tile
+ *            (row r, 16-byte chunk j at (r/8)*1024 + (r%8)*128 + ((j^(r%8))*16));
+ *            then the scales in [N/128, K/128] order.
+ * The packed buffer is read-only for the GEMM and can be shared by any number
+ * of concurrent calls.  Errors: ARG, SHAPE, ALIGN, WORKSPACE (too small), CUDA. */
+int fp8bs_prepack_weight(const uint8_t* wq, int64_t ldw, const void* ws, int64_t N, int64_t K,
+                         int scale_kind, void* packed, size_t packed_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused quant + block-scale GEMM ([P1] "Modifications": one launch per      */
+/* linear at M <= 32)                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Largest N of the fused GEMM (the workspace holds a fixed 32 KB region of
+ * per-n-tile counters, so one workspace serves weights of every shape). */
+#define FP8BS_MAX_FUSED_N 262144
+
+/* Workspace bytes the fused GEMM needs for an N x K weight on a device with
+ * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
+ * CUDA device).  Holds the device error word (256 B), the arrival counters
+ * (32 KB) and the fp32 split-K partial tiles (32 KB per CTA).  A workspace of
+ * the largest size over several shapes serves all of them.  Returns 0 for an
+ * invalid shape. */
+size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count);
+
+/* Zero a workspace before its first use (error word and counters).  The fused
+ * GEMM leaves the counters at zero again, so graph replays need no re-init. */
+int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Y = bf16(x W^T) with the 1x128 activation quant fused in.
+ *   x        : bf16 [M, K], row stride ldx; x and ldx*2 16-byte aligned.
+ *   M        : 1 .. FP8BS_MAX_M (0 enqueues nothing and returns FP8BS_OK).
+ *   N, K     : multiples of 128; N <= FP8BS_MAX_FUSED_N.
+ *   packed   : from fp8bs_prepack_weight with the same N, K and scale_kind;
+ *              packed_bytes its size (checked against N, K, kind on the host;
+ *              the header is checked on the device).
+ *   y        : bf16 [M, N], row stride ldy >= N (y and ldy*2 16-byte aligned).
+ *   workspace: >= fp8bs_workspace_bytes(N, K, 0) bytes, 256-byte aligned,
+ *              initialised once by fp8bs_workspace_init.  One workspace must not
+ *              be used by two calls that can run at the same time.
+ *   xq_out, xs_out : optional (NULL to skip) copies of the quantised
+ *              activations ([M, K] codes, row stride K; [M, K/128] scales),
+ *              bit-identical to fp8bs_quant.
+ * The result is deterministic: the split-K partials are summed in a fixed
+ * order, so repeated calls and graph replays give identical bits.
+ * Errors (host): ARG, SHAPE, ALIGN, WORKSPACE, CUDA.  Errors (device, via
+ * fp8bs_check_error): SCALE_KIND (header mismatch; y not written), TIMEOUT. */
+int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
+                     size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
+                     int64_t ldy, void* workspace, size_t workspace_bytes, uint8_t* xq_out,
+                     void* xs_out, void* stream);
+
+/* Synchronise `stream`, read the workspace error word, clear it, and return
+ * FP8BS_OK or the first device-side status recorded since the last check.
+ * After FP8BS_ERR_TIMEOUT the arrival counters may be left non-zero: call
+ * fp8bs_workspace_init before the workspace is used again. */
+int fp8bs_check_error(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

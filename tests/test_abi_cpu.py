@@ -1,0 +1,145 @@
+"""C ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host with the documented
+status codes (no device pointer is ever dereferenced on these paths)."""
+
+import ctypes
+
+import pytest
+
+import fp8_block_scale_x128_gb300 as fb
+
+OK, ARG, SHAPE, ALIGN, KIND, WS = 0, -1, -2, -3, -4, -5
+
+# fake but well-aligned device addresses: the host checks never touch them.
+# Every call below must be refused before any launch; as a second guard the
+# module never runs where a GPU is visible.
+P = 0x10000000
+STREAM = None
+
+pytestmark = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(),
+    reason="fake device pointers: host-check tests run only where no GPU is visible")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fb.build()
+    return fb.lib()
+
+
+def test_library_exports_every_declared_function(L):
+    names = fb.declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert fb.fp8bs_version() >> 16 == 1
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        assert fb.fp8bs_status_string(s) and fb.fp8bs_status_string(s) != "unknown status"
+    assert fb.fp8bs_status_string(-99) == "unknown status"
+
+
+def test_packed_weight_bytes(L):
+    # 256-byte header + 16 KB per tile + scales, rounded to 256
+    assert fb.fp8bs_packed_weight_bytes(5120, 4096, 0) == 256 + 40 * 32 * 16384 + 40 * 32 * 4
+    assert fb.fp8bs_packed_weight_bytes(5120, 4096, 1) == 256 + 40 * 32 * 16384 + 1280
+    assert fb.fp8bs_packed_weight_bytes(128, 128, 1) == 256 + 16384 + 256
+    assert fb.fp8bs_packed_weight_bytes(100, 128, 0) == 0
+    assert fb.fp8bs_packed_weight_bytes(128, 128, 7) == 0
+
+
+def test_workspace_bytes_for_explicit_sm_count(L):
+    fixed = 256 + 32768  # error word + counter region
+    # 152 SMs, 1280 units: one CTA per SM, two 16 KB partial slots each
+    assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == fixed + 152 * 2 * 128 * 32 * 4
+    # tiny problem: one CTA per unit
+    assert fb.fp8bs_workspace_bytes(128, 128, 152) == fixed + 1 * 2 * 16384
+    # many units: more CTAs than SMs (at most 10 units each)
+    n_big = fb.fp8bs_workspace_bytes(16384, 16384, 152)
+    assert n_big == fixed + ((16384 * 128 // 128 + 9) // 10) * 2 * 16384
+    assert fb.fp8bs_workspace_bytes(130, 128, 152) == 0
+    assert fb.fp8bs_workspace_bytes(262144, 128, 152) > 0
+    assert fb.fp8bs_workspace_bytes(262144 + 128, 128, 152) == 0
+
+
+def gemm(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K=4096, kind=0, y=P,
+         ldy=5120, ws=P, ws_bytes=1 << 30, xq=None, xs=None):
+    return L.fp8bs_gemm_fused(x, M, ldx, packed, packed_bytes, N, K, kind, y, ldy, ws, ws_bytes,
+                              xq, xs, STREAM)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=2), ARG),
+    (dict(M=33), SHAPE),
+    (dict(M=-1), SHAPE),
+    (dict(N=5000), SHAPE),
+    (dict(K=4000, ldx=4000), SHAPE),
+    (dict(N=0), SHAPE),
+    (dict(N=262144 + 128, ldy=262144 + 128), SHAPE),
+    (dict(x=None), ARG),
+    (dict(y=None), ARG),
+    (dict(ws=None), ARG),
+    (dict(packed=None), ARG),
+    (dict(ldx=4088), ARG),
+    (dict(ldy=5112), ARG),
+    (dict(x=P + 8), ALIGN),
+    (dict(ldx=4100), ALIGN),
+    (dict(y=P + 2), ALIGN),
+    (dict(packed=P + 16), ALIGN),
+    (dict(ws=P + 16), ALIGN),
+    (dict(xq=P + 4), ALIGN),
+    (dict(packed_bytes=1000), WS),
+])
+def test_gemm_fused_host_checks(L, kw, status):
+    assert gemm(L, **kw) == status
+
+
+def test_gemm_fused_empty_batch_is_a_no_op(L):
+    assert gemm(L, M=0, x=None, y=None) == OK
+
+
+def test_quant_host_checks(L):
+    q = L.fp8bs_quant
+    assert q(P, 2, 4096, 4096, 3, P, P, STREAM) == ARG
+    assert q(P, 2, 4000, 4000, 0, P, P, STREAM) == SHAPE
+    assert q(P, -1, 4096, 4096, 0, P, P, STREAM) == SHAPE
+    assert q(P, 0, 4096, 4096, 0, None, None, STREAM) == OK
+    assert q(None, 2, 4096, 4096, 0, P, P, STREAM) == ARG
+    assert q(P, 2, 4096, 2048, 0, P, P, STREAM) == ARG
+    assert q(P + 8, 2, 4096, 4096, 0, P, P, STREAM) == ALIGN
+    assert q(P, 2, 4096, 4100, 0, P, P, STREAM) == ALIGN
+    assert q(P, 2, 4096, 4096, 0, P, P + 2, STREAM) == ALIGN
+
+
+def test_prepack_and_weight_quant_host_checks(L):
+    pp = L.fp8bs_prepack_weight
+    assert pp(P, 4096, P, 5120, 4096, 5, P, 1 << 30, STREAM) == ARG
+    assert pp(P, 4096, P, 5100, 4096, 0, P, 1 << 30, STREAM) == SHAPE
+    assert pp(P, 4096, P, 5120, 4096, 0, P + 128, 1 << 30, STREAM) == ALIGN
+    assert pp(P, 4104, P, 5120, 4096, 0, P, 1 << 30, STREAM) == ALIGN
+    assert pp(P, 4096, P, 5120, 4096, 0, P, 1000, STREAM) == WS
+    qw = L.fp8bs_quant_weight
+    assert qw(P, 256, 256, 256, 9, P, P, STREAM) == ARG
+    assert qw(P, 256, 200, 256, 0, P, P, STREAM) == SHAPE
+    assert qw(P + 4, 256, 256, 256, 0, P, P, STREAM) == ALIGN
+
+
+def test_workspace_init_and_check_error_host_checks(L):
+    assert L.fp8bs_workspace_init(None, 1024, STREAM) == ARG
+    assert L.fp8bs_workspace_init(P + 16, 1024, STREAM) == ALIGN
+    assert L.fp8bs_workspace_init(P, 100, STREAM) == WS
+    assert L.fp8bs_check_error(None, STREAM) == ARG
+    assert L.fp8bs_check_error(P + 8, STREAM) == ALIGN
+    assert L.fp8bs_encode_e4m3(P, 6, P, STREAM) == SHAPE
+    assert L.fp8bs_encode_e4m3(P, 0, None, STREAM) == OK
+    assert L.fp8bs_encode_e4m3(P + 4, 8, P, STREAM) == ALIGN
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fb, "_lib", None)
+    monkeypatch.setattr(fb, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        fb.lib()
+    assert ctypes  # keep import used

@@ -1,0 +1,307 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Bar: bit-exact for every quantised byte and scale (activation quant, weight
+quant, the fused kernel's quant write-out, prepacked layout); the bf16 output
+within the tolerance in tests/helpers.py.  Inputs come from synth with the
+recipes of the pages' workloads; shapes span several tiles, ragged M and the
+full sizes of the benchmark."""
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scale_x128_gb300 as fb
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+F32, UE8 = fb.FP8BS_SCALE_F32, fb.FP8BS_SCALE_UE8M0
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fb.build()
+    fb.lib()
+    return torch.device("cuda", 0)
+
+
+def to_dev(a: np.ndarray, dev, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(dev)
+
+
+def x_dev(x_bits: np.ndarray, dev):
+    return to_dev(x_bits.view(np.int16), dev).view(torch.bfloat16)
+
+
+def run_fused(oracle_mod, dev, M, N, K, kind, seed, want_quant=True, ldx_pad=0, ldy_pad=0,
+              workspace=None):
+    x = synth.x_bf16(M, K, seed=seed)
+    wq, ws = H.weight(oracle_mod, N, K, kind, seed + 1)
+    y_ref, xq_ref, xs_ref = oracle_mod.linear(x, wq, ws, kind, nthreads=H.threads())
+    xd_full = torch.zeros((M, K + ldx_pad), dtype=torch.bfloat16, device=dev)
+    xd_full[:, :K] = x_dev(x, dev)
+    xd = xd_full[:, :K]
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind)
+    yd_full = torch.full((M, N + ldy_pad), float("nan"), dtype=torch.bfloat16, device=dev)
+    yd = yd_full[:, :N]
+    xq = torch.zeros((M, K), dtype=torch.uint8, device=dev) if want_quant else None
+    xs = (torch.zeros((M, K // 128), dtype=torch.uint8 if kind == UE8 else torch.float32,
+                      device=dev) if want_quant else None)
+    wsp = workspace if workspace is not None else fb.new_workspace(N, K, dev)
+    fb.fp8bs_gemm_fused(xd, packed, N, K, kind, y=yd, workspace=wsp, xq_out=xq, xs_out=xs)
+    assert fb.fp8bs_check_error(wsp) == 0
+    y = H.torch_u16_to_np(yd)
+    stats = H.check_y(y, y_ref, f"M={M} N={N} K={K} kind={kind}")
+    if ldy_pad:
+        assert torch.isnan(yd_full[:, N:].float()).all()  # nothing written past N
+    if want_quant:
+        assert np.array_equal(xq.cpu().numpy(), xq_ref)
+        assert np.array_equal(xs.cpu().numpy(), xs_ref)
+    return stats
+
+
+# ---------------------------------------------------------------------------
+# encoder: every fp32 bit pattern
+# ---------------------------------------------------------------------------
+
+def test_encode_e4m3_exhaustive_against_oracle(dev, oracle_mod):
+    chunk = 1 << 26
+    nthr = H.threads()
+    sub = chunk // nthr
+    pool = ThreadPoolExecutor(max_workers=nthr)
+    ref = np.empty(chunk, dtype=np.uint8)
+    base = torch.arange(chunk, dtype=torch.int64, device=dev)
+    for start in range(0, 1 << 32, chunk):
+        bits = (base + start).to(torch.int64)
+        bits = torch.where(bits >= (1 << 31), bits - (1 << 32), bits).to(torch.int32)
+        v = bits.view(torch.float32)
+        got = fb.fp8bs_encode_e4m3(v).cpu().numpy()
+        futs = [pool.submit(oracle_mod.e4m3_encode_bits, start + t * sub,
+                            sub if t < nthr - 1 else chunk - t * sub, ref[t * sub:])
+                for t in range(nthr)]
+        for f in futs:
+            f.result()
+        vv = np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        nan = np.isnan(vv)
+        bad = np.flatnonzero((got != ref) & ~nan)
+        assert bad.size == 0, f"first mismatch at bits {start + int(bad[0]):#010x}: " \
+                              f"gpu {got[bad[0]]:#04x} oracle {ref[bad[0]]:#04x}"
+        assert np.all((got[nan] & 0x7F) == 0x7F)
+    pool.shutdown()
+
+
+# ---------------------------------------------------------------------------
+# standalone quantisers
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("M,K,pad", [(1, 2048, 0), (3, 4096, 0), (9, 7168, 64), (17, 512, 8),
+                                     (32, 4096, 0), (33, 256, 0), (100, 1024, 0)])
+def test_quant_bit_exact(dev, oracle_mod, kind, M, K, pad):
+    x = synth.x_bf16(M, K, seed=7 * M + K)
+    xq_ref, xs_ref = oracle_mod.quant_1x128(x, kind)
+    full = torch.zeros((M, K + pad), dtype=torch.bfloat16, device=dev)
+    full[:, :K] = x_dev(x, dev)
+    xq, xs = fb.fp8bs_quant(full[:, :K], kind)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(xs.cpu().numpy(), xs_ref)
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+def test_quant_special_groups(dev, oracle_mod, kind):
+    K = 128 * 8
+    v = np.zeros((4, K), dtype=np.float32)
+    v[0, 128:256] = -0.0                        # zero group with negative zeros
+    v[0, 256:384] = 3.0                         # all equal
+    v[0, 384:512] = np.linspace(-1, 1, 128)     # plain
+    v[0, 512] = 3.0e38                          # huge
+    v[0, 513:640] = 1.0
+    v[1, :128] = np.float32(2.0 ** -130)        # bf16 subnormals
+    v[1, 5] = -np.float32(2.0 ** -133)
+    v[1, 128:256] = np.float32(448.0)
+    v[1, 129] = 17.0                            # exact tie at scale 1
+    v[2] = synth.bf16_bits_to_f32(synth.x_bf16(1, K, seed=3))[0] * np.float32(1e-30)
+    v[3] = synth.bf16_bits_to_f32(synth.x_bf16(1, K, seed=4))[0] * np.float32(1e30)
+    x = synth.f32_to_bf16_bits(v)
+    x[0, 128:256] = 0x8000
+    xq_ref, xs_ref = oracle_mod.quant_1x128(x, kind)
+    xq, xs = fb.fp8bs_quant(x_dev(x, dev), kind)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert np.array_equal(xs.cpu().numpy(), xs_ref)
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (4096, 2048)])
+def test_quant_weight_bit_exact(dev, oracle_mod, kind, N, K):
+    w = synth.w_f32(N, K, seed=N + K)
+    w[0, 0] = 0.0
+    if N >= 256:
+        w[128:256, :128] = 0.0                  # an all-zero block
+        w[130, 5] = -0.0
+    wq_ref, ws_ref = oracle_mod.quant_weight_128x128(w, kind)
+    wq, ws = fb.fp8bs_quant_weight(to_dev(w, dev), kind)
+    assert np.array_equal(wq.cpu().numpy(), wq_ref)
+    assert np.array_equal(ws.cpu().numpy(), ws_ref)
+
+
+# ---------------------------------------------------------------------------
+# prepack layout
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+def test_prepack_layout(dev, kind):
+    N, K = 384, 256
+    rng = np.random.default_rng(5)
+    wq = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    ws = (rng.random((N // 128, K // 128)).astype(np.float32) if kind == F32
+          else rng.integers(100, 140, size=(N // 128, K // 128), dtype=np.uint8))
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind).cpu().numpy()
+    hdr = packed[:32]
+    assert hdr[:4].tobytes() == b"F8BS"
+    assert int(hdr[8:16].view(np.int64)[0]) == N and int(hdr[16:24].view(np.int64)[0]) == K
+    assert int(hdr[24:28].view(np.int32)[0]) == kind
+    KB = K // 128
+    for nt in range(N // 128):
+        for kb in range(KB):
+            tile = packed[256 + (nt * KB + kb) * 16384:][:16384]
+            for r in range(128):
+                for j in range(8):
+                    off = (r // 8) * 1024 + (r % 8) * 128 + ((j ^ (r % 8)) * 16)
+                    src = wq[nt * 128 + r, kb * 128 + j * 16: kb * 128 + j * 16 + 16]
+                    assert np.array_equal(tile[off:off + 16], src)
+    sc = packed[256 + (N // 128) * KB * 16384:]
+    if kind == F32:
+        assert np.array_equal(sc[:ws.size * 4].view(np.float32), ws.ravel())
+    else:
+        assert np.array_equal(sc[:ws.size], ws.ravel())
+
+
+# ---------------------------------------------------------------------------
+# fused quant + GEMM
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 640), (1024, 1024), (640, 2048)])
+def test_fused_small_shapes(dev, oracle_mod, kind, M, N, K):
+    run_fused(oracle_mod, dev, M, N, K, kind, seed=M * 131 + N + K)
+
+
+@pytest.mark.parametrize("M", [1, 3, 4, 8, 9, 16, 17, 24, 32])
+def test_fused_m_sweep_5120x4096(dev, oracle_mod, M):
+    # the M sweep at N=5120, K=4096 with bit-exact quant bytes and scales
+    run_fused(oracle_mod, dev, M, 5120, 4096, F32, seed=1000 + M)
+
+
+def test_fused_smallest_4096x2048(dev, oracle_mod):
+    run_fused(oracle_mod, dev, 1, 4096, 2048, F32, seed=0)
+
+
+@pytest.mark.parametrize("N,K", [(5120, 4096), (4608, 4096), (4096, 2048)])
+@pytest.mark.parametrize("M", [1, 4, 8, 16, 32])
+def test_fused_projection_shapes(dev, oracle_mod, N, K, M):
+    run_fused(oracle_mod, dev, M, N, K, F32, seed=2000 + M + N // 128)
+
+
+@pytest.mark.parametrize("N,K", [(7168, 2048), (1536, 7168), (4096, 4096)])
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_fused_ue8m0_shapes(dev, oracle_mod, N, K, M):
+    run_fused(oracle_mod, dev, M, N, K, UE8, seed=3000 + M + N // 128)
+
+
+@pytest.mark.parametrize("M,kind", [(4, F32), (17, F32), (32, UE8)])
+def test_fused_more_ctas_than_sms(dev, oracle_mod, M, kind):
+    # 8192 units: more than one CTA per SM is needed (each keeps <= 12 tiles)
+    run_fused(oracle_mod, dev, M, 16384, 8192, kind, seed=4000 + M, want_quant=False)
+
+
+def test_fused_strided_x_and_y(dev, oracle_mod):
+    run_fused(oracle_mod, dev, 7, 640, 1024, F32, seed=11, ldx_pad=64, ldy_pad=24)
+
+
+def test_fused_workspace_reused_across_shapes(dev, oracle_mod):
+    ws = fb.new_workspace(16384, 8192, dev)
+    for (M, N, K) in [(3, 1024, 2048), (32, 5120, 4096), (1, 384, 640), (16, 4608, 4096)]:
+        run_fused(oracle_mod, dev, M, N, K, F32, seed=M + N, workspace=ws)
+
+
+def _setup(oracle_mod, dev, M, N, K, kind, seed):
+    x = synth.x_bf16(M, K, seed=seed)
+    wq, ws = H.weight(oracle_mod, N, K, kind, seed + 1)
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind)
+    return x, wq, ws, x_dev(x, dev), packed
+
+
+def test_fused_deterministic_and_graph_replay(dev, oracle_mod):
+    M, N, K = 9, 5120, 4096
+    x, wq, ws, xd, packed = _setup(oracle_mod, dev, M, N, K, F32, 77)
+    wsp = fb.new_workspace(N, K, dev)
+    outs = []
+    for _ in range(3):
+        y = fb.fp8bs_gemm_fused(xd, packed, N, K, F32, workspace=wsp)
+        outs.append(y.clone())
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    y_graph = torch.empty_like(outs[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fb.fp8bs_gemm_fused(xd, packed, N, K, F32, y=y_graph, workspace=wsp, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    y_graph.zero_()
+    with torch.cuda.graph(g):
+        fb.fp8bs_gemm_fused(xd, packed, N, K, F32, y=y_graph, workspace=wsp)
+    for _ in range(3):
+        y_graph.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph.view(torch.int16), outs[0].view(torch.int16))
+    assert fb.fp8bs_check_error(wsp) == 0
+
+
+def test_fused_rejects_mismatched_packed_weight(dev, oracle_mod):
+    M, N, K = 4, 256, 512
+    x, wq, ws, xd, packed = _setup(oracle_mod, dev, M, N, K, F32, 5)
+    wsp = fb.new_workspace(N, K, dev)
+    y = torch.full((M, N), 7.0, dtype=torch.bfloat16, device=dev)
+    # packed with fp32 scales, called as ue8m0: the device header check refuses
+    fb.fp8bs_gemm_fused(xd, packed, N, K, UE8, y=y, workspace=wsp)
+    assert fb.fp8bs_check_error(wsp) == -4
+    assert bool((y.float() == 7.0).all())
+    # called with another N: refused as well
+    y2 = torch.full((M, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    fb.fp8bs_gemm_fused(xd, packed, 128, K, F32, y=y2, workspace=wsp)
+    assert fb.fp8bs_check_error(wsp) == -4
+    assert bool((y2.float() == 7.0).all())
+    # and the error word was cleared: a good call reports ok
+    fb.fp8bs_gemm_fused(xd, packed, N, K, F32, y=y, workspace=wsp)
+    assert fb.fp8bs_check_error(wsp) == 0
+
+
+def test_fused_host_errors_raise(dev, oracle_mod):
+    M, N, K = 33, 256, 512
+    xd = torch.zeros((M, K), dtype=torch.bfloat16, device=dev)
+    packed = torch.zeros(fb.fp8bs_packed_weight_bytes(N, K, F32), dtype=torch.uint8, device=dev)
+    with pytest.raises(fb.Fp8bsError) as e:
+        fb.fp8bs_gemm_fused(xd, packed, N, K, F32)
+    assert e.value.status == -2
+    with pytest.raises(fb.Fp8bsError) as e:
+        fb.fp8bs_gemm_fused(xd[:4], packed[:1000], N, K, F32)
+    assert e.value.status == -5
+
+
+def test_binding_uses_native_library(dev):
+    maps = open(f"/proc/{os.getpid()}/maps").read()
+    assert "libfp8bs.so" in maps
