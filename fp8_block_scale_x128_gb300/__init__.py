@@ -25,6 +25,7 @@ import torch
 FP8BS_SCALE_F32 = 0
 FP8BS_SCALE_UE8M0 = 1
 FP8BS_MAX_M = 32
+FP8BS_FLAG_PDL = 1
 
 STATUS = {
     0: "FP8BS_OK", -1: "FP8BS_ERR_ARG", -2: "FP8BS_ERR_SHAPE", -3: "FP8BS_ERR_ALIGN",
@@ -82,8 +83,8 @@ def lib() -> ctypes.CDLL:
             "fp8bs_prepack_weight": ([vp, i64, vp, i64, i64, ci, vp, sz, vp], ci),
             "fp8bs_workspace_bytes": ([i64, i64, ci], sz),
             "fp8bs_workspace_init": ([vp, sz, vp], ci),
-            "fp8bs_gemm_fused": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, sz, vp, vp, vp],
-                                 ci),
+            "fp8bs_gemm_fused": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, sz, vp, vp,
+                                  c.c_uint, vp], ci),
             "fp8bs_check_error": ([vp, vp], ci),
         }
         for name, (args, res) in sig.items():
@@ -223,8 +224,14 @@ def new_workspace(N: int, K: int, device=None, stream=None) -> torch.Tensor:
 def fp8bs_gemm_fused(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
                      scale_kind: int = FP8BS_SCALE_F32, y: torch.Tensor | None = None,
                      workspace: torch.Tensor | None = None, xq_out: torch.Tensor | None = None,
-                     xs_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Y = bf16(quant(x) . W^T) for bf16 x [M <= 32, K] and a packed weight."""
+                     xs_out: torch.Tensor | None = None, pdl: bool = False,
+                     stream=None) -> torch.Tensor:
+    """Y = bf16(quant(x) . W^T) for bf16 x [M <= 32, K] and a packed weight.
+
+    pdl=True launches with programmatic dependent launch (FP8BS_FLAG_PDL); use
+    it only when the work just before this call on the stream does not write
+    `packed`.
+    """
     _require_cuda(x, packed, y, workspace, xq_out, xs_out)
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M = x.shape[0]
@@ -236,7 +243,7 @@ def fp8bs_gemm_fused(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
     rc = lib().fp8bs_gemm_fused(
         _ptr(x), M, x.stride(0), _ptr(packed), packed.numel(), N, K, int(scale_kind), _ptr(y),
         y.stride(0), _ptr(workspace), workspace.numel(), _ptr(xq_out), _ptr(xs_out),
-        _stream(stream))
+        FP8BS_FLAG_PDL if pdl else 0, _stream(stream))
     _check(rc, "fp8bs_gemm_fused")
     return y
 

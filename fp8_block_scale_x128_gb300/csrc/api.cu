@@ -49,10 +49,7 @@ int current_sm_count(int* out) {
     return FP8BS_OK;
 }
 
-size_t workspace_bytes_for(int64_t N, int64_t K, int sm_count) {
-    const size_t g = static_cast<size_t>(fused_max_grid(N, K, sm_count));
-    return ws_partials_offset() + g * 2 * kPartialSlotFloats * sizeof(float);
-}
+size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_count, K); }
 
 }  // namespace
 
@@ -129,9 +126,10 @@ int fp8bs_prepack_weight(const uint8_t* wq, int64_t ldw, const void* ws, int64_t
 }
 
 size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count) {
-    if (!nk_ok(N, K) || N > kMaxFusedN) return 0;
+    if (!nk_ok(N, K)) return 0;
     if (sm_count <= 0 && current_sm_count(&sm_count) != FP8BS_OK) return 0;
-    return workspace_bytes_for(N, K, sm_count);
+    if (!fused_shape_supported(N, K, sm_count)) return 0;
+    return workspace_bytes_for(K, sm_count);
 }
 
 int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -143,9 +141,9 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream) 
 
 int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* packed, size_t packed_bytes,
                      int64_t N, int64_t K, int scale_kind, uint16_t* y, int64_t ldy, void* workspace,
-                     size_t workspace_bytes, uint8_t* xq_out, void* xs_out, void* stream) {
-    if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;
-    if (M < 0 || M > FP8BS_MAX_M || !nk_ok(N, K) || N > kMaxFusedN) return FP8BS_ERR_SHAPE;
+                     size_t workspace_bytes, uint8_t* xq_out, void* xs_out, unsigned flags, void* stream) {
+    if (!kind_ok(scale_kind) || (flags & ~static_cast<unsigned>(FP8BS_FLAG_PDL)) != 0) return FP8BS_ERR_ARG;
+    if (M < 0 || M > FP8BS_MAX_M || !nk_ok(N, K)) return FP8BS_ERR_SHAPE;
     if (M == 0) return FP8BS_OK;
     if (!x || !packed || !y || !workspace) return FP8BS_ERR_ARG;
     if (ldx < K || ldy < N) return FP8BS_ERR_ARG;
@@ -157,7 +155,8 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     int sm = 0;
     const int rc = current_sm_count(&sm);
     if (rc != FP8BS_OK) return rc;
-    if (workspace_bytes < workspace_bytes_for(N, K, sm)) return FP8BS_ERR_WORKSPACE;
+    if (!fused_shape_supported(N, K, sm)) return FP8BS_ERR_SHAPE;
+    if (workspace_bytes < workspace_bytes_for(K, sm)) return FP8BS_ERR_WORKSPACE;
     FusedArgs a;
     a.x = x;
     a.ldx = ldx;
@@ -173,6 +172,7 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     a.xs_out = xs_out;
     a.sm_count = sm;
     a.timeout_cycles = kDefaultTimeoutCycles;
+    a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     return status_of(launch_fused(a, as_stream(stream)));
 }
 

@@ -33,32 +33,37 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
     return kHeaderBytes + static_cast<size_t>(N / kTile) * static_cast<size_t>(K / kTile) * kTileBytes;
 }
 
-// Workspace: [0, 256) error word (+ pad); [256, 256 + 32 KB) one u32 arrival
-// counter per (n-tile, 32-row quarter) -- a fixed region, so one workspace can
-// serve weights of any shape; then the split-K partial tiles, one 128 x 32
-// fp32 slot per (CTA, first/last n-tile of that CTA).
+// Workspace layout (bytes).  Every word the fused GEMM exchanges through it is
+// 64 bits: 32 data bits and the 32-bit epoch of the call that wrote it, so
+// words left by earlier calls (of any shape) are never taken for this call's
+// and nothing has to be cleared between calls.
+//   [0, 256)                    device error word
+//   [256, 256 + 4 KB)           epoch words, one per possible CTA index
+//   then sm_count x 32 KB       split-K partial slots (128 rows x 32 columns)
+//   then K/128 x 256 B          activation scales   [K/128][32 rows]
+//   then K/128 x 8 KB           activation codes    [K/128][32 rows][32 words of 4 codes]
 constexpr size_t kWsErrorBytes = 256;
-constexpr size_t kWsCounterBytes = 32768;
-constexpr int64_t kMaxFusedN = static_cast<int64_t>(kWsCounterBytes / (4 * sizeof(uint32_t))) * 128;
-constexpr size_t kPartialSlotFloats = 128 * 32;
+constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid (one CTA per SM)
+constexpr size_t kWsGenBytes = kMaxCtas * sizeof(uint32_t);
+constexpr size_t kSlotBytes = 128 * 32 * sizeof(uint64_t);
+constexpr size_t kXsRowBytes = 32 * sizeof(uint64_t);        // per K block
+constexpr size_t kXqRowBytes = 32 * 32 * sizeof(uint64_t);   // per K block
 
-__host__ __device__ inline size_t ws_counters_offset() { return kWsErrorBytes; }
-__host__ __device__ inline size_t ws_partials_offset() { return kWsErrorBytes + kWsCounterBytes; }
+__host__ __device__ inline size_t ws_gen_offset() { return kWsErrorBytes; }
+__host__ __device__ inline size_t ws_partials_offset() { return kWsErrorBytes + kWsGenBytes; }
+__host__ __device__ inline size_t ws_xs_offset(int sm_count) {
+    return ws_partials_offset() + static_cast<size_t>(sm_count) * kSlotBytes;
+}
+__host__ __device__ inline size_t ws_xq_offset(int sm_count, int64_t K) {
+    return ws_xs_offset(sm_count) + static_cast<size_t>(K / kTile) * kXsRowBytes;
+}
+__host__ __device__ inline size_t ws_total_bytes(int sm_count, int64_t K) {
+    return ws_xq_offset(sm_count, K) + static_cast<size_t>(K / kTile) * kXqRowBytes;
+}
 
 // Units of work per CTA the fused kernel keeps resident in shared memory.
 constexpr int kMaxUnitsM16 = 12;
 constexpr int kMaxUnitsM32 = 10;
-
-// Grid of the fused kernel for T = (N/128) * (K/128) units on sm_count SMs:
-// one CTA per SM when every CTA's share fits in shared memory, otherwise as
-// many CTAs as needed.  Units are split evenly (stream-K over n-major order).
-__host__ __device__ inline int fused_grid(int64_t T, int sm_count, int max_units) {
-    int64_t g = T < sm_count ? T : sm_count;
-    if (g < 1) g = 1;
-    int64_t need = (T + max_units - 1) / max_units;
-    if (need > g) g = need;
-    return static_cast<int>(g);
-}
 
 // Device error word: 0, or the negated status of the first fault.
 __device__ inline void record_error(uint32_t* err, int status) {
@@ -95,46 +100,6 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t byte) {
     return byte == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(byte << 23);
 }
 
-// Quantise one 1x128 group held by 16 consecutive lanes, 8 consecutive values
-// per lane (lane l of the half-warp holds k = 8l .. 8l+7).  Returns the 8 codes
-// packed little-endian (value 8l in bits 0-7 of .x), and the scale in
-// *scale_f32 (for ue8m0 also the byte in *scale_byte).  All 32 lanes of the
-// warp must call it (the two half-warps hold two independent groups).
-template <int KIND>
-__device__ __forceinline__ uint2 quant_group_16lanes(const float (&v)[8], float* scale_f32,
-                                                     uint32_t* scale_byte) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-#pragma unroll
-    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    const float s = __fdiv_rn(amax, 448.0f);
-    float scale = s;
-    if (KIND == FP8BS_SCALE_UE8M0) {
-        const uint32_t byte = e8m0_ceil_byte(s);
-        *scale_byte = byte;
-        scale = e8m0_to_float(byte);
-    }
-    *scale_f32 = scale;
-    uint2 c;
-    if (amax == 0.0f) {
-        // zero group: the signed zeros of x, no division
-        c.x = c.y = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            c.x |= (__float_as_uint(v[j]) >> 31) << (8 * j + 7);
-            c.y |= (__float_as_uint(v[j + 4]) >> 31) << (8 * j + 7);
-        }
-        return c;
-    }
-    float q[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], scale);
-    c.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-    c.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
-    return c;
-}
-
 __device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&v)[8]) {
     v[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
     v[1] = bf16_bits_to_float(raw.x >> 16);
@@ -144,6 +109,133 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&v)[8]) {
     v[5] = bf16_bits_to_float(raw.z >> 16);
     v[6] = bf16_bits_to_float(raw.w & 0xFFFFu);
     v[7] = bf16_bits_to_float(raw.w >> 16);
+}
+
+// Codes of the IEEE quotients RN32(v / scale) for the 8 bf16 values in raw.
+// Out of line, all arguments by value: the rare path of quant_slice.
+static __device__ __noinline__ uint2 e4m3_codes8_divide(uint4 raw, float scale) {
+    float v[8];
+    unpack_bf16x8(raw, v);
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], scale);
+    uint2 c;
+    c.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+    c.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
+    return c;
+}
+
+// Scale table.  A group maximum amax is a bf16 value m * 2^e with
+// m = 1 + i/128 (7 mantissa bits), so its scale RN32(amax / 448) equals
+// RN32(m / 448) * 2^e and the reciprocal RN32(1 / scale) equals
+// RN32(1 / RN32(m / 448)) * 2^-e -- exactly, while both are normal numbers
+// (biased exponent of amax >= 10).  tab[i] = {RN32(m / 448), RN32(1 / that)},
+// built with IEEE division by every block before it quantises.
+constexpr int kScaleTab = 128;
+
+__device__ __forceinline__ void fill_scale_table(float2* tab, int t, int nthreads) {
+    for (int i = t; i < kScaleTab; i += nthreads) {
+        const float m = 1.0f + static_cast<float>(i) * (1.0f / 128.0f);  // exact
+        const float sm = __fdiv_rn(m, 448.0f);
+        tab[i] = make_float2(sm, __frcp_rn(sm));
+    }
+}
+
+// True when the e4m3 code of a (an fp32 product within 2 ulps of the real
+// quotient t = x / scale) may differ from the code of q = RN32(t):
+//  * |a| in [2^-6, 512): e4m3 keeps 3 mantissa bits, so every rounding
+//    boundary (the midpoint of two neighbouring codes) has low 20 mantissa
+//    bits 0x80000.  q lies within 3 bit-steps of a inside a binade (5 across
+//    a binade edge, where no boundary is near), so an a more than 8 steps
+//    away from that pattern rounds like q;
+//  * 0 < |a| < 2^-6: the e4m3 subnormal range, where the boundary pattern
+//    moves with the exponent; rare, so such values take the exact path;
+//  * a = +-0 means x = +-0, whose code is exact.
+__device__ __forceinline__ bool e4m3_near_boundary(float a) {
+    const uint32_t mag = __float_as_uint(a) & 0x7FFFFFFFu;
+    const uint32_t low = (mag & 0xFFFFFu) - 0x80000u + 8u;  // in [0, 16] near the pattern
+    return mag != 0 && (mag < 0x3C800000u || low <= 16u);
+}
+
+// Result of quantising one 16-byte slice (8 values) of a 1x128 group.
+struct SliceQuant {
+    uint32_t lo, hi;  // 8 codes, little-endian (the slice's first value in bits 0-7 of lo)
+    float scale;      // the group scale (fp32; for ue8m0 the power of two)
+    uint32_t byte;    // ue8m0: the e8m0 byte of the scale
+};
+
+// Quantise one 1x128 group held by 16 consecutive lanes, 8 consecutive bf16
+// values per lane (lane l of the half-warp holds k = 8l .. 8l+7).  All 32
+// lanes of the warp must call it (each half-warp holds its own group).
+//
+// The codes are those of RN32(x / scale), found exactly without a division in
+// the common case: a = x * r with r = RN32(1 / scale) lies within 2 ulps of
+// the real quotient, and cvt(a) is the code of the correctly rounded quotient
+// unless a sits within a few bit-steps of an e4m3 rounding boundary
+// (e4m3_near_boundary, about 2^-16 of all values), where the IEEE quotient is
+// computed instead.  ue8m0 scales are powers of two, so there x * (1 / scale)
+// is the quotient itself.
+template <int KIND>
+__device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __restrict__ tab) {
+    float v[8];
+    unpack_bf16x8(raw, v);
+    const float m0 = fmaxf(fabsf(v[0]), fabsf(v[1])), m1 = fmaxf(fabsf(v[2]), fabsf(v[3]));
+    const float m2 = fmaxf(fabsf(v[4]), fabsf(v[5])), m3 = fmaxf(fabsf(v[6]), fabsf(v[7]));
+    const uint32_t mine = __float_as_uint(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+    // half-warp maxima (non-negative floats order like their bit patterns)
+    const bool low_half = (threadIdx.x & 31u) < 16u;
+    const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, low_half ? mine : 0u);
+    const uint32_t g1 = __reduce_max_sync(0xFFFFFFFFu, low_half ? 0u : mine);
+    const uint32_t amax_bits = low_half ? g0 : g1;
+    const float amax = __uint_as_float(amax_bits);
+    SliceQuant out;
+    out.byte = 0;
+    if (amax_bits == 0) {
+        // zero group: scale 0 (ue8m0: byte 0) and the signed zeros of x
+        out.scale = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(0u) : 0.0f;
+        out.lo = ((raw.x >> 15) & 1u) << 7 | ((raw.x >> 31) & 1u) << 15 | ((raw.y >> 15) & 1u) << 23 |
+                 ((raw.y >> 31) & 1u) << 31;
+        out.hi = ((raw.z >> 15) & 1u) << 7 | ((raw.z >> 31) & 1u) << 15 | ((raw.w >> 15) & 1u) << 23 |
+                 ((raw.w >> 31) & 1u) << 31;
+        return out;
+    }
+    const uint32_t e_biased = amax_bits >> 23;
+    float s, recip;
+    if (e_biased >= 10u) {
+        const float2 t = tab[(amax_bits >> 16) & 0x7Fu];
+        const int shift = (static_cast<int>(e_biased) - 127) * (1 << 23);
+        s = __int_as_float(__float_as_int(t.x) + shift);
+        recip = __int_as_float(__float_as_int(t.y) - shift);
+    } else {  // amax < 2^-117: scale and reciprocal leave the normal range
+        s = __fdiv_rn(amax, 448.0f);
+        recip = __frcp_rn(s);
+    }
+    if (KIND == FP8BS_SCALE_UE8M0) {
+        out.byte = e8m0_ceil_byte(s);
+        out.scale = e8m0_to_float(out.byte);
+        recip = e8m0_to_float(254u - out.byte);  // 2^(127 - e): exact
+    } else {
+        out.scale = s;
+    }
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = v[j] * recip;
+    bool exact = KIND == FP8BS_SCALE_UE8M0;
+    if (!exact) {
+        bool near = !(amax >= 0x1p-100f);  // tiny groups: 1 / scale may overflow
+#pragma unroll
+        for (int j = 0; j < 8; ++j) near |= e4m3_near_boundary(a[j]);
+        exact = !near;
+    }
+    if (exact) {
+        out.lo = e4m3x2(a[0], a[1]) | (e4m3x2(a[2], a[3]) << 16);
+        out.hi = e4m3x2(a[4], a[5]) | (e4m3x2(a[6], a[7]) << 16);
+    } else {
+        const uint2 c = e4m3_codes8_divide(raw, s);
+        out.lo = c.x;
+        out.hi = c.y;
+    }
+    return out;
 }
 
 // ---------------------------------------------------------------------------
@@ -171,11 +263,14 @@ struct FusedArgs {
     void* xs_out;
     int sm_count;
     long long timeout_cycles;
+    int pdl;
 };
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream);
 
-// Largest grid the fused kernel uses for an N x K weight on sm_count SMs.
-int fused_max_grid(int64_t N, int64_t K, int sm_count);
+// Whether the fused GEMM supports an N x K weight on sm_count SMs: one CTA per
+// SM at most, so the K blocks of one n-tile must fit the resident units of
+// all SMs.
+bool fused_shape_supported(int64_t N, int64_t K, int sm_count);
 
 }  // namespace fp8bs

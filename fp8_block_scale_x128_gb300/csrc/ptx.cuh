@@ -83,6 +83,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialization) start once every CTA of this grid has executed this.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the previous kernel on the stream has completed and its memory
+// operations are visible (a no-op without programmatic serialization).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // tcgen05 (TMEM and the 5th-generation MMA)
 // ---------------------------------------------------------------------------
 

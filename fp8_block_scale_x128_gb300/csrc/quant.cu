@@ -24,6 +24,9 @@ template <int KIND>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_1x128_kernel(const uint16_t* __restrict__ x, int M, int K, int64_t ldx,
                        uint8_t* __restrict__ xq, void* __restrict__ xs) {
+    __shared__ float2 tab[kScaleTab];
+    fill_scale_table(tab, threadIdx.x, kQuantWarps * 32);
+    __syncthreads();
     const int l16 = threadIdx.x & 15;
     const int KB = K / kTile;
     const int64_t groups = static_cast<int64_t>(M) * KB;
@@ -38,11 +41,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         const int kb = valid ? static_cast<int>(g % KB) : 0;
         uint4 raw = make_uint4(0, 0, 0, 0);
         if (valid) raw = *reinterpret_cast<const uint4*>(x + m * ldx + kb * kTile + 8 * l16);
-        float v[8];
-        unpack_bf16x8(raw, v);
-        float sf;
-        uint32_t sb = 0;
-        const uint2 codes = quant_group_16lanes<KIND>(v, &sf, &sb);
+        const SliceQuant qs = quant_slice<KIND>(raw, tab);
+        const uint2 codes = make_uint2(qs.lo, qs.hi);
+        const float sf = qs.scale;
+        const uint32_t sb = qs.byte;
         if (valid) {
             *reinterpret_cast<uint2*>(xq + static_cast<int64_t>(m) * K + kb * kTile + 8 * l16) = codes;
             if (l16 == 0) {

@@ -149,26 +149,39 @@ int fp8bs_prepack_weight(const uint8_t* wq, int64_t ldw, const void* ws, int64_t
 /* linear at M <= 32)                                                        */
 /* ------------------------------------------------------------------------ */
 
-/* Largest N of the fused GEMM (the workspace holds a fixed 32 KB region of
- * per-n-tile counters, so one workspace serves weights of every shape). */
-#define FP8BS_MAX_FUSED_N 262144
+/* Flags of fp8bs_gemm_fused. */
+enum {
+    /* Launch with programmatic dependent launch: the call may start, and read
+     * `packed`, while the kernel before it on the stream is still running; x,
+     * y, xq_out, xs_out and the workspace are touched only after that kernel
+     * has completed.  Back-to-back linears then overlap one call's start-up
+     * and weight stream with the previous call's tail.  Use it only when the
+     * work just before this call on the stream does not write `packed`. */
+    FP8BS_FLAG_PDL = 1u,
+};
 
 /* Workspace bytes the fused GEMM needs for an N x K weight on a device with
  * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
- * CUDA device).  Holds the device error word (256 B), the arrival counters
- * (32 KB) and the fp32 split-K partial tiles (32 KB per CTA).  A workspace of
- * the largest size over several shapes serves all of them.  Returns 0 for an
- * invalid shape. */
+ * CUDA device): a 256-byte error word, 4 KB of epoch words, one 32 KB split-K
+ * slot per multiprocessor and 8.25 KB per 128 columns of K for the quantised
+ * activations the CTAs exchange.  The size depends on K and sm_count only and
+ * every region sits at the same place for every N, so a workspace sized for
+ * the largest K serves every weight of that K or less.  Returns 0 for an
+ * unsupported shape (K/128 must not exceed 10 * sm_count). */
 size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count);
 
-/* Zero a workspace before its first use (error word and counters).  The fused
- * GEMM leaves the counters at zero again, so graph replays need no re-init. */
+/* Zero a workspace before its first use.  The fused GEMM tags every word it
+ * exchanges through the workspace with a per-call epoch kept in the workspace
+ * itself, so later calls and graph replays need no re-init. */
 int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Y = bf16(x W^T) with the 1x128 activation quant fused in.
  *   x        : bf16 [M, K], row stride ldx; x and ldx*2 16-byte aligned.
  *   M        : 1 .. FP8BS_MAX_M (0 enqueues nothing and returns FP8BS_OK).
- *   N, K     : multiples of 128; N <= FP8BS_MAX_FUSED_N.
+ *   N, K     : multiples of 128 with K/128 <= 10 * (multiprocessor count).
+ *              Weights with more than 10 * (multiprocessor count) 128x128
+ *              tiles are processed in several launches of whole 128-row
+ *              slices.
  *   packed   : from fp8bs_prepack_weight with the same N, K and scale_kind;
  *              packed_bytes its size (checked against N, K, kind on the host;
  *              the header is checked on the device).
@@ -179,18 +192,23 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *   xq_out, xs_out : optional (NULL to skip) copies of the quantised
  *              activations ([M, K] codes, row stride K; [M, K/128] scales),
  *              bit-identical to fp8bs_quant.
+ *   flags    : 0 or FP8BS_FLAG_PDL.
  * The result is deterministic: the split-K partials are summed in a fixed
  * order, so repeated calls and graph replays give identical bits.
+ * The CTAs of one launch exchange data, so a call assumes the whole device:
+ * one CTA per multiprocessor, all resident together.  (Under a partition of
+ * the GPU with fewer multiprocessors the bounded waits expire and the call
+ * reports FP8BS_ERR_TIMEOUT.)
  * Errors (host): ARG, SHAPE, ALIGN, WORKSPACE, CUDA.  Errors (device, via
  * fp8bs_check_error): SCALE_KIND (header mismatch; y not written), TIMEOUT. */
 int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
                      size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
                      int64_t ldy, void* workspace, size_t workspace_bytes, uint8_t* xq_out,
-                     void* xs_out, void* stream);
+                     void* xs_out, unsigned flags, void* stream);
 
 /* Synchronise `stream`, read the workspace error word, clear it, and return
  * FP8BS_OK or the first device-side status recorded since the last check.
- * After FP8BS_ERR_TIMEOUT the arrival counters may be left non-zero: call
+ * After FP8BS_ERR_TIMEOUT the epoch words may disagree: call
  * fp8bs_workspace_init before the workspace is used again. */
 int fp8bs_check_error(void* workspace, void* stream);
 

@@ -51,23 +51,23 @@ def test_packed_weight_bytes(L):
 
 
 def test_workspace_bytes_for_explicit_sm_count(L):
-    fixed = 256 + 32768  # error word + counter region
-    # 152 SMs, 1280 units: one CTA per SM, two 16 KB partial slots each
-    assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == fixed + 152 * 2 * 128 * 32 * 4
-    # tiny problem: one CTA per unit
-    assert fb.fp8bs_workspace_bytes(128, 128, 152) == fixed + 1 * 2 * 16384
-    # many units: more CTAs than SMs (at most 10 units each)
-    n_big = fb.fp8bs_workspace_bytes(16384, 16384, 152)
-    assert n_big == fixed + ((16384 * 128 // 128 + 9) // 10) * 2 * 16384
+    def expect(K, sm):
+        return 256 + 4096 + sm * 128 * 32 * 8 + (K // 128) * (32 * 8 + 32 * 32 * 8)
+    assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == expect(4096, 152)
+    assert fb.fp8bs_workspace_bytes(128, 128, 152) == expect(128, 152)
+    # independent of N
+    assert fb.fp8bs_workspace_bytes(16384, 4096, 152) == expect(4096, 152)
     assert fb.fp8bs_workspace_bytes(130, 128, 152) == 0
-    assert fb.fp8bs_workspace_bytes(262144, 128, 152) > 0
-    assert fb.fp8bs_workspace_bytes(262144 + 128, 128, 152) == 0
+    # one n-tile's K blocks must fit 10 units per SM
+    assert fb.fp8bs_workspace_bytes(128, 1520 * 128, 152) == expect(1520 * 128, 152)
+    assert fb.fp8bs_workspace_bytes(128, 1521 * 128, 152) == 0
+    assert fb.fp8bs_workspace_bytes(128, 128, 2000) == 0
 
 
 def gemm(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K=4096, kind=0, y=P,
-         ldy=5120, ws=P, ws_bytes=1 << 30, xq=None, xs=None):
+         ldy=5120, ws=P, ws_bytes=1 << 30, xq=None, xs=None, flags=0):
     return L.fp8bs_gemm_fused(x, M, ldx, packed, packed_bytes, N, K, kind, y, ldy, ws, ws_bytes,
-                              xq, xs, STREAM)
+                              xq, xs, flags, STREAM)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -77,7 +77,8 @@ def gemm(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K=4096, 
     (dict(N=5000), SHAPE),
     (dict(K=4000, ldx=4000), SHAPE),
     (dict(N=0), SHAPE),
-    (dict(N=262144 + 128, ldy=262144 + 128), SHAPE),
+    (dict(N=(1 << 24) + 128, ldy=(1 << 24) + 128), SHAPE),
+    (dict(flags=2), ARG),
     (dict(x=None), ARG),
     (dict(y=None), ARG),
     (dict(ws=None), ARG),

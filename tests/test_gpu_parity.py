@@ -118,6 +118,21 @@ def test_quant_bit_exact(dev, oracle_mod, kind, M, K, pad):
 
 
 @pytest.mark.parametrize("kind", [F32, UE8])
+def test_quant_bit_exact_16m_values(dev, oracle_mod, kind):
+    # 16M values: the quantiser's reciprocal fast path meets a few hundred
+    # quotients within a few ulps of an e4m3 rounding boundary, where it must
+    # fall back to the IEEE division
+    M, K = 4096, 4096
+    x = synth.x_bf16(M, K, seed=2024 + kind)
+    xq_ref, xs_ref = oracle_mod.quant_1x128(x, kind)
+    xq, xs = fb.fp8bs_quant(x_dev(x, dev), kind)
+    assert np.array_equal(xs.cpu().numpy(), xs_ref)
+    got = xq.cpu().numpy()
+    bad = np.argwhere(got != xq_ref)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[0]}"
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
 def test_quant_special_groups(dev, oracle_mod, kind):
     K = 128 * 8
     v = np.zeros((4, K), dtype=np.float32)
@@ -219,9 +234,10 @@ def test_fused_ue8m0_shapes(dev, oracle_mod, N, K, M):
     run_fused(oracle_mod, dev, M, N, K, UE8, seed=3000 + M + N // 128)
 
 
-@pytest.mark.parametrize("M,kind", [(4, F32), (17, F32), (32, UE8)])
-def test_fused_more_ctas_than_sms(dev, oracle_mod, M, kind):
-    # 8192 units: more than one CTA per SM is needed (each keeps <= 12 tiles)
+@pytest.mark.parametrize("M,kind", [(4, F32), (9, F32), (17, F32), (32, UE8)])
+def test_fused_weight_larger_than_one_launch(dev, oracle_mod, M, kind):
+    # 8192 units: more than one CTA per SM can hold, so the call runs several
+    # launches of whole 128-row slices
     run_fused(oracle_mod, dev, M, 16384, 8192, kind, seed=4000 + M, want_quant=False)
 
 
@@ -268,6 +284,89 @@ def test_fused_deterministic_and_graph_replay(dev, oracle_mod):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(y_graph.view(torch.int16), outs[0].view(torch.int16))
+    assert fb.fp8bs_check_error(wsp) == 0
+
+
+def test_fused_pdl_independent_calls_match_plain_launches(dev, oracle_mod):
+    # back-to-back calls on different weights, launched with programmatic
+    # dependent launch inside a CUDA graph, give the same bits as plain calls
+    for M in (5, 17):
+        N, K = 4608, 4096
+        x = synth.x_bf16(M, K, seed=91 + M)
+        xd = x_dev(x, dev)
+        packs = []
+        for c in range(4):
+            wq, ws = H.weight(oracle_mod, N, K, F32, 500 + c)
+            packs.append(fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), F32))
+        wsp = fb.new_workspace(N, K, dev)
+        plain = [fb.fp8bs_gemm_fused(xd, pk, N, K, F32, workspace=wsp).clone() for pk in packs]
+        ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in packs]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for pk, y in zip(packs, ys):
+                fb.fp8bs_gemm_fused(xd, pk, N, K, F32, y=y, workspace=wsp, pdl=True, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for a, b in zip(plain, ys):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for pk, y in zip(packs, ys):
+                fb.fp8bs_gemm_fused(xd, pk, N, K, F32, y=y, workspace=wsp, pdl=True)
+        for _ in range(3):
+            for y in ys:
+                y.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            for a, b in zip(plain, ys):
+                assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert fb.fp8bs_check_error(wsp) == 0
+
+
+@pytest.mark.parametrize("kind,M", [(F32, 8), (F32, 24), (UE8, 8)])
+def test_fused_pdl_dependent_chain(dev, oracle_mod, kind, M):
+    # each layer's output is the next layer's input: with programmatic
+    # dependent launch the consumer must still see the producer's y
+    D, layers = 2048, 6
+    x0 = synth.x_bf16(M, D, seed=7)
+    packs, wts = [], []
+    for layer in range(layers):
+        wq, ws = H.weight(oracle_mod, D, D, kind, 600 + layer)
+        wts.append((wq, ws))
+        packs.append(fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind))
+    wsp = fb.new_workspace(D, D, dev)
+    acts = [x_dev(x0, dev)] + [torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+                               for _ in range(layers)]
+
+    def run(pdl):
+        for layer in range(layers):
+            fb.fp8bs_gemm_fused(acts[layer], packs[layer], D, D, kind, y=acts[layer + 1],
+                                workspace=wsp, pdl=pdl)
+        torch.cuda.synchronize()
+        return [a.clone() for a in acts[1:]]
+
+    plain = run(False)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for layer in range(layers):
+            fb.fp8bs_gemm_fused(acts[layer], packs[layer], D, D, kind, y=acts[layer + 1],
+                                workspace=wsp, pdl=True)
+    for _ in range(3):
+        for a in acts[1:]:
+            a.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(plain, acts[1:]):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # every layer matches the oracle applied to the GPU's own input
+    prev = x0
+    for layer in range(layers):
+        wq, ws = wts[layer]
+        y_ref, _, _ = oracle_mod.linear(prev, wq, ws, kind, nthreads=H.threads())
+        got = H.torch_u16_to_np(plain[layer])
+        H.check_y(got, y_ref, f"layer {layer}")
+        prev = got
     assert fb.fp8bs_check_error(wsp) == 0
 
 
