@@ -299,7 +299,8 @@ def cpu_baseline(calls, budget_s: float):
 class Step:
     """Packed weights, activations and the CUDA graph of one step."""
 
-    def __init__(self, fb, torch, calls, dev, stream, io: bool = False, graph: bool = True):
+    def __init__(self, fb, torch, calls, dev, stream, io: bool = False, graph: bool = True,
+                 pdl: bool = True):
         import synth
         self.calls = calls
         self.packs = {}
@@ -323,6 +324,7 @@ class Step:
         self.y = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                   for (M, N, K, _k, _w) in calls}
         self.io = io
+        self.pdl = pdl
         if io:
             self.x_host = [torch.empty((c[0], c[2]), dtype=torch.bfloat16).pin_memory()
                            for c in calls]
@@ -332,6 +334,9 @@ class Step:
                            for c in calls]
         self.stream = stream
         self.fb = fb
+        # weights, x and the workspace's initial zeros were written on the current
+        # stream; `stream` does not wait for it, so finish them before any call
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             self.enqueue()  # eager pass: module load, kernel attributes
         stream.synchronize()
@@ -357,7 +362,7 @@ class Step:
             if self.io:
                 x.copy_(self.x_host[i], non_blocking=True)
             self.fb.fp8bs_gemm_fused(x, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
-                                     workspace=self.workspace, stream=self.stream)
+                                     workspace=self.workspace, pdl=self.pdl, stream=self.stream)
             if self.io:
                 self.y_host[i].copy_(y, non_blocking=True)
 
@@ -380,19 +385,28 @@ def time_steps(torch, step: Step, steps: int, warmup: int, world: int, dev) -> f
     return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
 
-def per_m_table(fb, torch, dev, stream):
+def per_m_table(fb, torch, dev, stream, pdl):
     """us/call and GB/s per M at N=5120 K=4096 (graph of 24 rotated calls)."""
     out = {}
     for M in M_SWEEP:
-        st = Step(fb, torch, [(M, 5120, 4096, 0, c) for c in range(COPIES)], dev, stream)
+        st = Step(fb, torch, [(M, 5120, 4096, 0, c) for c in range(COPIES)], dev, stream, pdl=pdl)
+        progress(f"per-M step M={M}")
         reps = 50
         ms = time_steps(torch, st, reps, 5, 1, dev)
+        rc = fb.fp8bs_check_error(st.workspace, stream)
+        if rc != 0:
+            raise SystemExit(f"per-M step M={M}: device error {fb.fp8bs_status_string(rc)}")
         us = ms * 1e3 / (reps * COPIES)
         out[str(M)] = {"us": round(us, 3),
                        "GBps": round(algorithmic_bytes(M, 5120, 4096, 0) / us / 1e3, 1)}
         del st
     torch.cuda.empty_cache()
     return out
+
+
+def progress(msg: str) -> None:
+    if os.environ.get("FP8BS_BENCH_VERBOSE"):
+        print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
 
 
 def run_gpu(args):
@@ -412,8 +426,11 @@ def run_gpu(args):
     step_bytes = sum(algorithmic_bytes(M, N, K, kind) for (M, N, K, kind, _) in calls)
     weight_bytes = sum(N * K for (N, K, _k, _w) in {c[1:] for c in calls})
 
-    st = Step(fb, torch, calls, dev, stream, graph=not args.no_graph)
+    pdl = not args.no_pdl
+    progress("building the step (weights, graph)")
+    st = Step(fb, torch, calls, dev, stream, graph=not args.no_graph, pdl=pdl)
     with ClockSampler(local) as clk:
+        progress("timed region")
         ms = time_steps(torch, st, args.steps, args.warmup, world, dev)
     clocks = clk.summary()
     sec = ms / 1e3
@@ -428,7 +445,8 @@ def run_gpu(args):
 
     # end to end through the public call with host buffers: every call copies
     # its x from pinned host memory and its y back, inside the timed region
-    st_io = Step(fb, torch, calls, dev, stream, io=True)
+    progress("end-to-end step")
+    st_io = Step(fb, torch, calls, dev, stream, io=True, pdl=pdl)
     e2e_steps = max(3, args.steps // 4)
     ms_io = time_steps(torch, st_io, e2e_steps, min(args.warmup, 10), world, dev)
     e2e_value = world * step_bytes * e2e_steps / (ms_io / 1e3) / 1e9
@@ -439,7 +457,8 @@ def run_gpu(args):
 
     per_m = None
     if args.workload == "msweep" and rank == 0 and not args.no_per_m:
-        per_m = per_m_table(fb, torch, dev, stream)
+        progress("per-M table")
+        per_m = per_m_table(fb, torch, dev, stream, pdl)
 
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -465,6 +484,7 @@ def run_gpu(args):
                        "graph": ("eager launches" if args.no_graph
                                  else "one CUDA graph replay per step"),
                        "parallelism": "replicas",
+                       "pdl": pdl,
                        "per_m_us_and_GBps": per_m},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),
@@ -495,6 +515,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-m", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="plain launches instead of programmatic dependent launch")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every call eagerly instead of replaying a CUDA graph")
     args = ap.parse_args(argv)
