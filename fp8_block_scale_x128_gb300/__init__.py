@@ -26,6 +26,8 @@ FP8BS_SCALE_F32 = 0
 FP8BS_SCALE_UE8M0 = 1
 FP8BS_MAX_M = 32
 FP8BS_FLAG_PDL = 1
+FP8BS_STATIC_MAX_K = 16384
+FP8BS_STATIC_MAX_SMS = 160
 
 STATUS = {
     0: "FP8BS_OK", -1: "FP8BS_ERR_ARG", -2: "FP8BS_ERR_SHAPE", -3: "FP8BS_ERR_ALIGN",
@@ -86,6 +88,8 @@ def lib() -> ctypes.CDLL:
             "fp8bs_gemm_fused": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, sz, vp, vp,
                                   c.c_uint, vp], ci),
             "fp8bs_check_error": ([vp, vp], ci),
+            "fp8bs_gemm_fused_static": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, vp, vp,
+                                         c.c_uint, vp], ci),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -245,6 +249,30 @@ def fp8bs_gemm_fused(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         y.stride(0), _ptr(workspace), workspace.numel(), _ptr(xq_out), _ptr(xs_out),
         FP8BS_FLAG_PDL if pdl else 0, _stream(stream))
     _check(rc, "fp8bs_gemm_fused")
+    return y
+
+
+def fp8bs_gemm_fused_static(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
+                            scale_kind: int = FP8BS_SCALE_F32, y: torch.Tensor | None = None,
+                            xq_out: torch.Tensor | None = None, xs_out: torch.Tensor | None = None,
+                            status_out: torch.Tensor | None = None, pdl: bool = False,
+                            stream=None) -> torch.Tensor:
+    """fp8bs_gemm_fused with the library's fixed per-device scratch instead of a
+    workspace (K <= FP8BS_STATIC_MAX_K).  The C call allocates nothing; pass
+    `y` to keep this wrapper from allocating it.  `status_out` (int32 [1] on
+    the device, optional) receives the sticky device status after the kernel.
+    """
+    _require_cuda(x, packed, y, xq_out, xs_out, status_out)
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M = x.shape[0]
+    assert x.shape[1] == K
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    rc = lib().fp8bs_gemm_fused_static(
+        _ptr(x), M, x.stride(0), _ptr(packed), packed.numel(), N, K, int(scale_kind), _ptr(y),
+        y.stride(0), _ptr(xq_out), _ptr(xs_out), _ptr(status_out),
+        FP8BS_FLAG_PDL if pdl else 0, _stream(stream))
+    _check(rc, "fp8bs_gemm_fused_static")
     return y
 
 

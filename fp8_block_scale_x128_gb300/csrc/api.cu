@@ -12,6 +12,8 @@
 // for dense 128x128 fp8 linears (6/8)", "Modifications" requires.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace {
@@ -50,6 +52,42 @@ int current_sm_count(int* out) {
 }
 
 size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_count, K); }
+
+// Scratch of fp8bs_gemm_fused_static: one fixed array per device, laid out like
+// a caller's workspace for FP8BS_STATIC_MAX_SMS CTAs and K up to
+// FP8BS_STATIC_MAX_K.
+constexpr size_t kStaticScratchBytes =
+    kWsErrorBytes + kWsGenBytes + static_cast<size_t>(FP8BS_STATIC_MAX_SMS) * kSlotBytes +
+    static_cast<size_t>(FP8BS_STATIC_MAX_K / kTile) * (kXsRowBytes + kXqRowBytes);
+// The error word and the epoch words are the part that must start at zero;
+// every other word is tagged with the epoch of the call that wrote it.
+static_assert(kStaticScratchBytes == 6328576, "fp8bs.h states the scratch size");
+constexpr size_t kStaticZeroBytes = kWsErrorBytes + kWsGenBytes;
+
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kStaticMaxDevices = 64;
+std::mutex g_static_mu;
+uint8_t* g_static_ptr[kStaticMaxDevices] = {};
+
+// Address of the current device's scratch; the first call per device looks it
+// up and zeroes its head on `s`, then waits for that, so a call from another
+// thread or stream never sees a half-cleared scratch.
+int static_scratch(cudaStream_t s, uint8_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
+    if (dev < 0 || dev >= kStaticMaxDevices) return FP8BS_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return FP8BS_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, kStaticZeroBytes, s) != cudaSuccess) return FP8BS_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return FP8BS_ERR_CUDA;
+        g_static_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_static_ptr[dev];
+    return FP8BS_OK;
+}
 
 }  // namespace
 
@@ -174,6 +212,52 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     a.timeout_cycles = kDefaultTimeoutCycles;
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     return status_of(launch_fused(a, as_stream(stream)));
+}
+
+int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
+                            size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
+                            int64_t ldy, uint8_t* xq_out, void* xs_out, uint32_t* status_out,
+                            unsigned flags, void* stream) {
+    if (!kind_ok(scale_kind) || (flags & ~static_cast<unsigned>(FP8BS_FLAG_PDL)) != 0) return FP8BS_ERR_ARG;
+    if (M < 0 || M > FP8BS_MAX_M || !nk_ok(N, K)) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !packed || !y) return FP8BS_ERR_ARG;
+    if (ldx < K || ldy < N) return FP8BS_ERR_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(y, 16) || ldy % 8 != 0 || !aligned(packed, 256) ||
+        (xq_out && !aligned(xq_out, 16)) || (xs_out && scale_kind == FP8BS_SCALE_F32 && !aligned(xs_out, 4)) ||
+        (status_out && !aligned(status_out, 4)))
+        return FP8BS_ERR_ALIGN;
+    if (packed_bytes < fp8bs_packed_weight_bytes(N, K, scale_kind)) return FP8BS_ERR_WORKSPACE;
+    if (K > FP8BS_STATIC_MAX_K) return FP8BS_ERR_WORKSPACE;
+    int sm = 0;
+    int rc = current_sm_count(&sm);
+    if (rc != FP8BS_OK) return rc;
+    if (sm > FP8BS_STATIC_MAX_SMS) sm = FP8BS_STATIC_MAX_SMS;
+    if (!fused_shape_supported(N, K, sm)) return FP8BS_ERR_SHAPE;
+    if (workspace_bytes_for(K, sm) > kStaticScratchBytes) return FP8BS_ERR_WORKSPACE;
+    uint8_t* scratch = nullptr;
+    rc = static_scratch(as_stream(stream), &scratch);
+    if (rc != FP8BS_OK) return rc;
+    FusedArgs a;
+    a.x = x;
+    a.ldx = ldx;
+    a.packed = static_cast<const uint8_t*>(packed);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.kind = scale_kind;
+    a.y = y;
+    a.ldy = ldy;
+    a.workspace = scratch;
+    a.xq_out = xq_out;
+    a.xs_out = xs_out;
+    a.sm_count = sm;
+    a.timeout_cycles = kDefaultTimeoutCycles;
+    a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
+    rc = status_of(launch_fused(a, as_stream(stream)));
+    if (rc != FP8BS_OK || !status_out) return rc;
+    return status_of(cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
+                                     as_stream(stream)));
 }
 
 int fp8bs_check_error(void* workspace, void* stream) {

@@ -26,7 +26,8 @@
  * Conventions for every entry point:
  *   - Data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates no memory, keeps no pointer after a call returns and never
- *     synchronises, except fp8bs_check_error (documented there).
+ *     synchronises, except fp8bs_check_error and the first call of
+ *     fp8bs_gemm_fused_static on each device (both documented there).
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Work is enqueued on it; results are ready when it reaches them.
  *   - Return value: FP8BS_OK (0) or a negative fp8bs_status.  Argument faults
@@ -211,6 +212,44 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
  * After FP8BS_ERR_TIMEOUT the epoch words may disagree: call
  * fp8bs_workspace_init before the workspace is used again. */
 int fp8bs_check_error(void* workspace, void* stream);
+
+/* Limits of fp8bs_gemm_fused_static's fixed scratch. */
+#define FP8BS_STATIC_MAX_K 16384  /* largest K it accepts                   */
+#define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */
+
+/* fp8bs_gemm_fused without a workspace argument: the scratch lives in one
+ * fixed device array inside this library (6,328,576 bytes per device,
+ * sized for FP8BS_STATIC_MAX_SMS CTAs and K up to FP8BS_STATIC_MAX_K), so the
+ * call allocates no device memory, ever.  It is meant for callers that cannot
+ * allocate or own device memory: an operator plugged into a runtime whose
+ * device memory is handed out up front to its own pool (a serving engine that
+ * reserves all free HBM for its KV cache), a callback that gets no allocator
+ * handle, or a latency-critical path where an allocation's implicit device
+ * synchronisation is not acceptable.  The pages describe no counterpart: it is
+ * a deployment convenience around the same kernel.
+ *
+ * Arguments, results and host checks are those of fp8bs_gemm_fused, except:
+ *   K > FP8BS_STATIC_MAX_K is refused with FP8BS_ERR_WORKSPACE (the scratch
+ *   is too small); on a device with more than FP8BS_STATIC_MAX_SMS
+ *   multiprocessors the call uses that many CTAs.
+ *   status_out: optional (NULL to skip) device uint32 that receives, in stream
+ *   order after the kernel, the scratch's error word: 0, or the negated
+ *   status (FP8BS_ERR_TIMEOUT, FP8BS_ERR_SCALE_KIND) of the first device-side
+ *   failure of any call on this device.  The word is sticky: this entry point
+ *   cannot re-initialise the shared scratch, so after a timeout its epoch
+ *   words may disagree and later calls may time out too.
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's address with cudaGetSymbolAddress, zeroes its error and epoch
+ * words on `stream` and waits for that; make the first call before any stream
+ * capture.
+ * Sharing: every call on one device uses the same array, so two calls that
+ * can overlap (different streams, different host threads without ordering)
+ * race and may time out or return wrong results.  Calls in order on one
+ * stream, with or without FP8BS_FLAG_PDL, are safe. */
+int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
+                            size_t packed_bytes, int64_t N, int64_t K, int scale_kind,
+                            uint16_t* y, int64_t ldy, uint8_t* xq_out, void* xs_out,
+                            uint32_t* status_out, unsigned flags, void* stream);
 
 #ifdef __cplusplus
 }

@@ -101,6 +101,35 @@ def test_gemm_fused_empty_batch_is_a_no_op(L):
     assert gemm(L, M=0, x=None, y=None) == OK
 
 
+def gemm_static(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K=4096, kind=0,
+                y=P, ldy=5120, xq=None, xs=None, status=None, flags=0):
+    return L.fp8bs_gemm_fused_static(x, M, ldx, packed, packed_bytes, N, K, kind, y, ldy, xq, xs,
+                                     status, flags, STREAM)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=2), ARG),
+    (dict(flags=2), ARG),
+    (dict(M=33), SHAPE),
+    (dict(N=5000), SHAPE),
+    (dict(x=None), ARG),
+    (dict(packed=None), ARG),
+    (dict(y=None), ARG),
+    (dict(ldy=5112), ARG),
+    (dict(x=P + 8), ALIGN),
+    (dict(status=P + 2), ALIGN),
+    (dict(packed_bytes=1000), WS),
+    # one K block past the fixed scratch's limit
+    (dict(K=fb.FP8BS_STATIC_MAX_K + 128, ldx=fb.FP8BS_STATIC_MAX_K + 128), WS),
+])
+def test_gemm_fused_static_host_checks(L, kw, status):
+    assert gemm_static(L, **kw) == status
+
+
+def test_gemm_fused_static_empty_batch_is_a_no_op(L):
+    assert gemm_static(L, M=0, x=None, y=None) == OK
+
+
 def test_quant_host_checks(L):
     q = L.fp8bs_quant
     assert q(P, 2, 4096, 4096, 3, P, P, STREAM) == ARG
