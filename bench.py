@@ -33,6 +33,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -49,7 +50,7 @@ COPIES = 24
 KERNEL_SOURCES = ["fp8_block_scale_x128_gb300/csrc/gemm_fused.cu",
                   "fp8_block_scale_x128_gb300/csrc/ptx.cuh",
                   "fp8_block_scale_x128_gb300/csrc/internal.cuh"]
-DRAM_PROFILE = os.path.join(ROOT, "profiles", "fused_quant_gemm_5120x4096_msweep_dram.json")
+DRAM_PROFILE = os.path.join(ROOT, "profiles", "fused_quant_gemm_5120x4096_msweep_dram.md")
 
 
 def algorithmic_bytes(M: int, N: int, K: int, kind: int) -> int:
@@ -103,12 +104,24 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def bench_config(desc: str, calls) -> dict:
+    """The workload description both arms report."""
+    weight_bytes = sum(N * K for (N, K, _k, _w) in {c[1:] for c in calls})
+    return {"workload": desc, "calls_per_step": len(calls),
+            "l2": "inputs larger than L2 (rotated weight copies, "
+                  f"{weight_bytes // 10**6} MB of distinct weights per step vs 129 MB)",
+            "parallelism": "replicas"}
+
+
 def dram_traffic_per_launch(workload: str):
     """Per-launch DRAM bytes of the fused kernel from the committed ncu summary,
     or None when the kernel source has changed since the counters were taken."""
     try:
         with open(DRAM_PROFILE) as f:
-            prof = json.load(f)
+            # "- key: value" lines of the summary
+            prof = dict(m.groups() for m in re.finditer(r"^- (\w+): (\S+)\s*$", f.read(), re.M))
+        if "bytes_per_launch_mean" in prof:
+            prof["bytes_per_launch_mean"] = float(prof["bytes_per_launch_mean"])
     except (OSError, ValueError):
         return None
     if prof.get("kernel_src_sha256") != kernel_source_hash() or workload != "msweep":
@@ -266,7 +279,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": desc},
+        "data": "synthetic", "config": bench_config(desc, calls),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
                          "sample": smp.sample_desc(1)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -424,8 +437,6 @@ def run_gpu(args):
     desc, calls = workload_plan(args.workload)
     stream = torch.cuda.Stream(device=dev)
     step_bytes = sum(algorithmic_bytes(M, N, K, kind) for (M, N, K, kind, _) in calls)
-    weight_bytes = sum(N * K for (N, K, _k, _w) in {c[1:] for c in calls})
-
     pdl = not args.no_pdl
     progress("building the step (weights, graph)")
     st = Step(fb, torch, calls, dev, stream, graph=not args.no_graph, pdl=pdl)
@@ -478,14 +489,11 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 x e4m3 -> f32 (bf16 in, bf16 out)", "data": "synthetic",
             "us_per_call": ms * 1e3 / launches,
-            "config": {"workload": desc, "calls_per_step": len(calls),
-                       "l2": "inputs larger than L2 (rotated weight copies, "
-                             f"{weight_bytes // 10**6} MB of distinct weights per step vs 129 MB)",
-                       "graph": ("eager launches" if args.no_graph
+            "config": bench_config(desc, calls),
+            "launch": {"graph": ("eager launches" if args.no_graph
                                  else "one CUDA graph replay per step"),
-                       "parallelism": "replicas",
-                       "pdl": pdl,
-                       "per_m_us_and_GBps": per_m},
+                       "pdl": pdl},
+            "per_m_us_and_GBps": per_m,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),
                          "peak_source": peak_src, "kernel": "fused_quant_gemm_kernel",

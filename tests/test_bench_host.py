@@ -1,0 +1,63 @@
+"""Host logic of bench.py's multi-rank path, on CPU with gloo (world size 2):
+rendezvous from the launcher's environment, the barrier, the maximum over
+ranks of the timed region, and rank 0 alone running the reference arm."""
+
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "WORLD_SIZE": str(world),
+                       "RANK": str(rank), "LOCAL_RANK": str(rank)})
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+
+    import bench
+    w, r, local = bench.dist_setup()
+    assert (w, r, local) == (world, rank, rank)
+    bench.barrier(w)
+    # rank r "measured" 10 + r ms: every rank must report the slowest one
+    got = bench.max_over_ranks(10.0 + rank, w, torch.device("cpu"))
+    with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+        json.dump({"max": got}, f)
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2(tmp_path):
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True,
+                       start_method="spawn")
+    for r in range(2):
+        with open(tmp_path / f"rank{r}.json") as f:
+            assert json.load(f)["max"] == 11.0
+
+
+def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_bench_rejects_short_warmup():
+    sys.path.insert(0, ROOT)
+    import bench
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
