@@ -56,13 +56,8 @@ size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_c
 // Scratch of fp8bs_gemm_fused_static: one fixed array per device, laid out like
 // a caller's workspace for FP8BS_STATIC_MAX_SMS CTAs and K up to
 // FP8BS_STATIC_MAX_K.
-constexpr size_t kStaticScratchBytes =
-    kWsErrorBytes + kWsGenBytes + static_cast<size_t>(FP8BS_STATIC_MAX_SMS) * kSlotBytes +
-    static_cast<size_t>(FP8BS_STATIC_MAX_K / kTile) * (kXsRowBytes + kXqRowBytes);
-// The error word and the epoch words are the part that must start at zero;
-// every other word is tagged with the epoch of the call that wrote it.
-static_assert(kStaticScratchBytes == 6328576, "fp8bs.h states the scratch size");
-constexpr size_t kStaticZeroBytes = kWsErrorBytes + kWsGenBytes;
+constexpr size_t kStaticScratchBytes = ws_total_bytes(FP8BS_STATIC_MAX_SMS, FP8BS_STATIC_MAX_K);
+static_assert(kStaticScratchBytes == 3199232, "fp8bs.h states the scratch size");
 
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -71,8 +66,9 @@ std::mutex g_static_mu;
 uint8_t* g_static_ptr[kStaticMaxDevices] = {};
 
 // Address of the current device's scratch; the first call per device looks it
-// up and zeroes its head on `s`, then waits for that, so a call from another
-// thread or stream never sees a half-cleared scratch.
+// up and zeroes it on `s` (the error word, the epoch words and every flag must
+// start at zero), then waits for that, so a call from another thread or stream
+// never sees a half-cleared scratch.
 int static_scratch(cudaStream_t s, uint8_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
@@ -81,7 +77,7 @@ int static_scratch(cudaStream_t s, uint8_t** out) {
     if (!g_static_ptr[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return FP8BS_ERR_CUDA;
-        if (cudaMemsetAsync(p, 0, kStaticZeroBytes, s) != cudaSuccess) return FP8BS_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, kStaticScratchBytes, s) != cudaSuccess) return FP8BS_ERR_CUDA;
         if (cudaStreamSynchronize(s) != cudaSuccess) return FP8BS_ERR_CUDA;
         g_static_ptr[dev] = static_cast<uint8_t*>(p);
     }

@@ -11,84 +11,80 @@
 //
 // Work unit: one (n-tile of 128 weight rows, 128-wide K block) = one 16 KB fp8
 // weight tile.  The T = N/128 * K/128 units, in n-major order, are split evenly
-// over at most one CTA per SM ("stream-K"): CTA c owns units [c*T/G, (c+1)*T/G)
-// -- at most 10-12, all resident in shared memory -- and all CTAs of the grid
-// are resident at once.  Every CTA:
-//   1. issues a bulk async copy (TMA, evict-first) for EVERY weight tile it
-//      owns at once, so the HBM stream starts in the first microsecond;
-//   2. gets the quantised activations of its units' K blocks into the
-//      shared-memory B operands (K-major, 128-byte swizzle):
-//        - up to 8 tokens it quantises them itself (M x units groups);
-//        - above that every CTA quantises 1/G of all M x K/128 groups and
-//          publishes them in the workspace as 64-bit (4 codes, epoch) words,
-//          and each CTA copies the words of its units' K blocks -- the
-//          quantisation is then done once per group instead of once per CTA;
-//   3. two threads (warps 1 and 3) issue, per unit, four tcgen05.mma
-//      kind::f8f6f4 (K = 32 each) with the weight tile as the 128-row A
-//      operand and the tokens as N = 16 or 32 ("swap-AB"), each unit into a
-//      TMEM accumulator of its own;
-//   4. four epilogue warps (one per 32 TMEM lanes) read each unit's fp32
-//      128 x N block, multiply by xs[m,kb] * ws[nt,kb] in fp32 and accumulate
-//      in registers (the per-K-block rescale of the page);
-//   5. an n-tile whose whole K range the CTA owns is written as bf16 Y.
-//      Otherwise the CTA holding the tile's first unit reduces it: the other
-//      contributors publish their fp32 partials as (value, epoch) words and
-//      exit; the reducer sums its own and their partials in CTA order -- a
+// over at most one CTA per SM ("stream-K"): CTA c owns units [c*T/G, (c+1)*T/G),
+// at most 10-12.  A CTA needs about 110 KB of shared memory and 128 registers
+// per thread, so two fit on an SM: with programmatic dependent launch the next
+// call's CTAs stream their weights while this call's CTAs finish.
+//   1. Weight ring: one thread keeps 4-5 tiles in flight with bulk async
+//      copies (TMA, evict-first), refilling a slot as soon as the MMAs that
+//      read it complete.  The first tiles go out at entry, before the wait for
+//      the previous kernel: they read only the packed weight.
+//   2. Activations into the shared-memory B operands (K-major, 128-byte
+//      swizzle), for all of the CTA's units:
+//        - up to 8 tokens every CTA quantises its own units' groups;
+//        - above that each 1x128 group is quantised once, by one CTA, and
+//          published in the workspace (codes, scale, then a flag set to the
+//          call's epoch); a CTA copies the groups of its units with cp.async
+//          once their flags carry the epoch.
+//   3. One thread issues, per unit, four tcgen05.mma kind::f8f6f4 (K = 32
+//      each) with the weight tile as the 128-row A operand and the tokens as
+//      N = 16 or 32 ("swap-AB"), into one of 4 TMEM accumulator stages.
+//   4. Four epilogue warps (one per 32 TMEM lanes) read each accumulator,
+//      free its stage, and accumulate P * (xs[m,kb] * ws[nt,kb]) in fp32
+//      registers (the per-K-block rescale of the page).
+//   5. An n-tile whose whole K range the CTA owns is written as bf16 Y.
+//      Otherwise the tile's first CTA reduces it: each later contributor
+//      writes its fp32 partial into its slot and sets the slot's flags; the
+//      reducer copies the partials (cp.async) and sums them in CTA order -- a
 //      fixed order, so results are deterministic -- and writes bf16 Y.
 // A call's epoch is one more than the workspace's epoch word for the CTA's
-// index, and every CTA moves the words of its index class on to it when it
-// ends, so all words stay equal and every word written by an earlier call
-// carries an older epoch.
-// With programmatic dependent launch the next call's CTAs start while this
-// one finishes: everything before griddepcontrol.wait reads only the packed
-// weight; x, y and the workspace are touched after it.
+// index; every CTA moves the words of its index class on to it when it ends,
+// so all words stay equal and every flag set by an earlier call is older.
 // Every wait is bounded; on expiry the kernel records FP8BS_ERR_TIMEOUT in the
 // workspace error word, drains its own copies and MMAs (again bounded), frees
-// TMEM and returns.
+// TMEM and returns.  The code of each role is kept small (rolled loops): the
+// instruction footprint, not the arithmetic, bounds these short phases.
 #include "internal.cuh"
 #include "ptx.cuh"
 
 namespace fp8bs {
 namespace {
 
-// 8 warps.  Warp 0: weight copies (one thread), then quant.  Warps 1 and 3:
-// MMA issue (even / odd units); warp 3 first builds the scale table.  Warp 2:
-// unit info and header check, then quant.  Warps 4-7: quant, then the
-// epilogue (one warp per 32 TMEM lanes).
+// 8 warps.  Warp 0: weight ring (one thread).  Warp 1: TMEM and MMA issue
+// (one thread).  Warp 2: unit info and header check, then quant.  Warp 3:
+// scale table, then quant.  Warps 4-7: quant, then the epilogue (one warp per
+// 32 TMEM lanes).
 constexpr int kThreads = 256;
-constexpr int kQuantThreads = kThreads - 64;  // all warps but the two MMA warps
+constexpr int kQuantThreads = 192;  // warps 2-7
 constexpr int kQuantHalfWarps = kQuantThreads / 16;
 constexpr int kLocalMaxM = 8;  // up to this many tokens every CTA quantises its own groups
-
-__device__ __forceinline__ bool is_mma_warp(int warp) { return warp == 1 || warp == 3; }
-// index of a quantising thread: warps 0, 2, 4, 5, 6, 7 -> 0 .. kQuantThreads-1
-__device__ __forceinline__ int quant_index(int tid) {
-    const int warp = tid >> 5;
-    return warp == 0 ? tid : warp == 2 ? tid - 32 : tid - 64;
-}
+constexpr int kAccStages = 4;
+constexpr uint32_t kMaxSmemPerCta = 112 * 1024;  // two CTAs per SM
 
 template <int MPAD, bool DIST>
 struct Cfg {
     static constexpr int kUnits = MPAD == 16 ? kMaxUnitsM16 : kMaxUnitsM32;
-    static constexpr int kRows = DIST ? MPAD : kLocalMaxM;  // largest M of this variant
+    static constexpr int kStages = MPAD == 16 ? 5 : 4;
     static constexpr uint32_t kBBytes = MPAD * 128;  // activation operand of one unit
-    static constexpr uint32_t kTmemCols = MPAD == 16 ? 256 : 512;
-    static constexpr uint32_t kOffW = 0;
-    static constexpr uint32_t kOffB = kOffW + kUnits * kTileBytes;
+    static constexpr uint32_t kTmemCols = kAccStages * MPAD;
+    static constexpr uint32_t kRingBytes = kStages * kTileBytes;
+    static constexpr uint32_t kOffB = kRingBytes;
     static constexpr uint32_t kOffXs = kOffB + kUnits * kBBytes;
     static constexpr uint32_t kOffWs = kOffXs + kUnits * MPAD * 4;
     static constexpr uint32_t kOffKb = kOffWs + kUnits * 4;
     static constexpr uint32_t kOffTab = (kOffKb + kUnits * 4 + 15) / 16 * 16;
     static constexpr uint32_t kOffBar = kOffTab + kScaleTab * 8;
-    static constexpr uint32_t kOffMisc = kOffBar + 3 * kUnits * 8 + 8;  // + the header barrier
+    // full[S], empty[S], accf[A], acce[A], bready[U], hdr
+    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAccStages + kUnits + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
-    // 16-byte activation slices per quantising thread: units * rows * 16
-    static constexpr int kSlices = (kUnits * kRows * 16 + kQuantThreads - 1) / kQuantThreads;
-    // scale words per quantising thread (exchange variant): units * rows
-    static constexpr int kScaleSlices = (kUnits * kRows + kQuantThreads - 1) / kQuantThreads;
-    static_assert(kUnits * MPAD <= static_cast<int>(kTmemCols), "TMEM columns");
-    static_assert(kSmem <= 232448, "shared memory per CTA");
+    // local quant: groups (unit, token) per half-warp
+    static constexpr int kGroupsPerHw = (kUnits * kLocalMaxM + kQuantHalfWarps - 1) / kQuantHalfWarps;
+    // exchange: groups (unit, token) per quantising thread
+    static constexpr int kGroupsPerThread = (kUnits * MPAD + kQuantThreads - 1) / kQuantThreads;
+    static_assert(kSmem <= kMaxSmemPerCta, "shared memory per CTA");
     static_assert(kBBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
+    static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
 };
 
 struct Params {
@@ -104,16 +100,16 @@ struct Params {
     int64_t ldy;
     uint32_t* err;
     uint32_t* gen;            // epoch words
-    uint64_t* ll;             // split-K slots: [grid][128 rows][32 cols] (value, epoch)
-    uint64_t* xsw;            // activation scales: [K/128][32 rows] (scale bits, epoch)
-    uint64_t* xqw;            // activation codes: [K/128][32 rows][32] (4 codes, epoch)
+    uint32_t* pflag;          // partial flags [CTA][4 epilogue warps]
+    float* slots;             // partial slots [CTA][32 columns][128 rows]
+    uint8_t* act;             // activation records [K/128][kKbRecBytes]
     uint8_t* xq_out;
     void* xs_out;
     long long timeout;
     int pdl;
 };
 
-enum : int { kMiscTmem = 0, kMiscAbort = 1, kMiscHdrOk = 2, kMiscIssued = 3 };
+enum : int { kMiscTmem = 0, kMiscAbort = 1, kMiscHdrOk = 2, kMiscIssued = 3, kMiscCommitted = 4 };
 
 __device__ __forceinline__ uint32_t unit_begin(uint32_t c, uint32_t T, uint32_t G) {
     return static_cast<uint32_t>(static_cast<uint64_t>(c) * T / G);
@@ -132,98 +128,54 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return r;
 }
 
-__device__ __forceinline__ void st_pair(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+__device__ __forceinline__ uint32_t* kb_flags(const Params& p, uint32_t kb) {
+    return reinterpret_cast<uint32_t*>(p.act + kb * kKbRecBytes + kKbRecFlags);
+}
+__device__ __forceinline__ uint32_t* kb_scales(const Params& p, uint32_t kb) {
+    return reinterpret_cast<uint32_t*>(p.act + kb * kKbRecBytes + kKbRecScales);
+}
+__device__ __forceinline__ uint8_t* kb_codes(const Params& p, uint32_t kb) { return p.act + kb * kKbRecBytes + kKbRecCodes; }
+
+// Cold path of every bounded wait.
+__device__ __noinline__ void raise_timeout(uint32_t* err, volatile uint32_t* misc) {
+    record_error(err, FP8BS_ERR_TIMEOUT);
+    misc[kMiscAbort] = 1;
 }
 
-__device__ __forceinline__ void st_word(uint64_t* p, uint64_t a) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
-}
-
-__device__ __forceinline__ void ld_pair(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
-    uint64_t a;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
-    return a;
-}
-
-__device__ __forceinline__ uint32_t ld_u32_gpu(const uint32_t* p) {
-    uint32_t a;
-    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(a) : "l"(p) : "memory");
-    return a;
-}
-
-__device__ __forceinline__ uint64_t tag(uint32_t data, uint32_t epoch) {
-    return static_cast<uint64_t>(data) | (static_cast<uint64_t>(epoch) << 32);
-}
-
-__device__ __forceinline__ bool tagged(uint64_t w, uint32_t epoch) { return static_cast<uint32_t>(w >> 32) == epoch; }
-
-__device__ __forceinline__ bool timed_out(long long t0, long long timeout, volatile uint32_t* misc, uint32_t* err) {
-    if (misc[kMiscAbort] != 0) return true;
-    if (clock64() - t0 > timeout) {
-        record_error(err, FP8BS_ERR_TIMEOUT);
-        misc[kMiscAbort] = 1;
-        return true;
-    }
-    return false;
-}
-
-// Bounded wait by a single thread.  Returns false when the deadline passes
-// (recording FP8BS_ERR_TIMEOUT and raising the CTA's abort flag) or, with
-// honour_abort, when another role has already raised it.
-__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, long long timeout,
-                                        volatile uint32_t* misc, uint32_t* err, bool honour_abort) {
+// Bounded wait for an mbarrier phase by one thread: false on expiry (recorded)
+// or once the CTA has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, volatile uint32_t* misc) {
+    if (ptx::mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
-    while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && misc[kMiscAbort] != 0) return false;
-        if (clock64() - t0 > timeout) {
-            record_error(err, FP8BS_ERR_TIMEOUT);
-            misc[kMiscAbort] = 1;
+    while (!ptx::mbar_test(bar, parity)) {
+        if (misc[kMiscAbort] != 0) return false;
+        if (clock64() - t0 > p.timeout) {
+            raise_timeout(p.err, misc);
             return false;
         }
     }
+    return true;
 }
 
-struct WordPair {
-    uint64_t a, b;
-    bool ok;
-};
-
-// Re-reads a pair of exchange words (first read: a, b) until both carry the
-// epoch (bounded; .ok false on expiry).  All by value: nothing goes through
-// memory.
-__device__ __noinline__ WordPair poll_pair(const uint64_t* p, uint64_t a, uint64_t b, uint32_t epoch,
-                                           long long timeout, volatile uint32_t* misc, uint32_t* err) {
+// Teardown drain: ignores the abort flag, still bounded.
+__device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, long long timeout) {
     const long long t0 = clock64();
-    WordPair r{a, b, true};
-    while (!(tagged(r.a, epoch) && tagged(r.b, epoch))) {
-        if (timed_out(t0, timeout, misc, err)) {
-            r.ok = false;
-            return r;
-        }
-        ld_pair(p, r.a, r.b);
+    while (!ptx::mbar_test(bar, parity) && clock64() - t0 <= timeout) {
     }
-    return r;
 }
 
-// The same for a single word.
-__device__ __noinline__ WordPair poll_word(const uint64_t* p, uint64_t a, uint32_t epoch, long long timeout,
-                                           volatile uint32_t* misc, uint32_t* err) {
+// Bounded wait until a flag carries the epoch (acquire), by one thread.
+__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t epoch, const Params& p, volatile uint32_t* misc) {
+    if (ptx::ld_acquire_u32(f) == epoch) return true;
     const long long t0 = clock64();
-    WordPair r{a, 0, true};
-    while (!tagged(r.a, epoch)) {
-        if (timed_out(t0, timeout, misc, err)) {
-            r.ok = false;
-            return r;
+    while (ptx::ld_acquire_u32(f) != epoch) {
+        if (misc[kMiscAbort] != 0) return false;
+        if (clock64() - t0 > p.timeout) {
+            raise_timeout(p.err, misc);
+            return false;
         }
-        r.a = ld_word(p);
     }
-    return r;
+    return true;
 }
 
 template <int MPAD>
@@ -235,64 +187,73 @@ __device__ __forceinline__ void store_y(const Params& p, int n, const float (&v)
 
 // Output of one n-tile's accumulator by one epilogue warp (rows q*32 .. +31).
 // role 0: this CTA owns the tile's whole K range -> bf16 Y.
-// role 1: a later contributor -> publish the partial in this CTA's slot.
-// role 2: the reducer -> wait for the other contributors' partials, sum in CTA
-//         order, bf16 Y.
-template <int MPAD>
-__device__ __forceinline__ void flush_tile(const Params& p, uint32_t nt, const float (&acc)[MPAD], uint32_t c,
-                                           uint32_t G, int role, int q, int lane, uint32_t epoch,
-                                           volatile uint32_t* misc) {
+// role 1: a later contributor -> write the partial of these rows into this
+//         CTA's slot, then set this warp's flag.
+// role 2: the reducer -> copy the later contributors' partials of these rows
+//         (in batches that fit this warp's quarter of the idle weight ring),
+//         sum in CTA order, bf16 Y.
+// Returns false if a wait gave up.
+template <int MPAD, int STAGE_FLOATS>
+__device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (&acc)[MPAD], uint32_t c, uint32_t G,
+                                        int role, int q, int lane, uint32_t epoch, volatile uint32_t* misc,
+                                        float* stage) {
     const int r = q * 32 + lane;
     const int n = static_cast<int>(nt) * kTile + r;
-    const int pairs = (p.M + 1) >> 1;
     if (role == 0) {
         store_y<MPAD>(p, n, acc);
-        return;
+        return true;
     }
     if (role == 1) {
-        uint64_t* slot = p.ll + (static_cast<size_t>(c) * 128 + r) * 32;
+        float* slot = p.slots + static_cast<size_t>(c) * (32 * 128);
 #pragma unroll
-        for (int j = 0; j < MPAD / 2; ++j)
-            if (j < pairs)
-                st_pair(slot + 2 * j, tag(__float_as_uint(acc[2 * j]), epoch),
-                        tag(__float_as_uint(acc[2 * j + 1]), epoch));
-        return;
+        for (int m = 0; m < MPAD; ++m)
+            if (m < p.M) slot[m * 128 + r] = acc[m];
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) ptx::st_release_u32(p.pflag + c * 4 + q, epoch);
+        return true;
     }
-    float sum[MPAD];
-#pragma unroll
-    for (int m = 0; m < MPAD; ++m) sum[m] = acc[m];
     const uint32_t last = cta_of((nt + 1) * static_cast<uint32_t>(p.KB) - 1, p.T, G);
-    for (uint32_t cc = c + 1; cc <= last; ++cc) {  // fixed order: deterministic
-        const uint64_t* slot = p.ll + (static_cast<size_t>(cc) * 128 + r) * 32;
-        uint64_t w[MPAD];
-#pragma unroll
-        for (int j = 0; j < MPAD / 2; ++j) {  // all words of this contributor in flight at once
-            if (j < pairs) ld_pair(slot + 2 * j, w[2 * j], w[2 * j + 1]);
-            else w[2 * j] = w[2 * j + 1] = tag(0, epoch);
+    const int per = p.M * 32;               // floats per contributor (this warp's rows)
+    const int batch = STAGE_FLOATS / per;   // contributors per batch (>= 4)
+    float* st = stage + q * STAGE_FLOATS;   // this warp's quarter of the ring
+#pragma unroll 1
+    for (uint32_t b = c + 1; b <= last; b += batch) {
+        const int nb = static_cast<int>(last + 1 - b) < batch ? static_cast<int>(last + 1 - b) : batch;
+        bool ok = true;
+        if (lane < nb) ok = wait_flag(p.pflag + (b + lane) * 4 + q, epoch, p, misc);
+        if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+        // 16-byte chunks: (contributor j, column m, rows 4k .. 4k+3 of this warp)
+#pragma unroll 1
+        for (int t = lane; t < nb * p.M * 8; t += 32) {
+            const int jm = t >> 3, k = t & 7;
+            const int j = jm / p.M;
+            const int m = jm - j * p.M;
+            ptx::cp_async16(st + jm * 32 + 4 * k,
+                            p.slots + static_cast<size_t>(b + j) * (32 * 128) + m * 128 + q * 32 + 4 * k);
         }
+        ptx::cp_async_wait_all();
+        __syncwarp();
+#pragma unroll 1
+        for (int j = 0; j < nb; ++j) {
 #pragma unroll
-        for (int j = 0; j < MPAD / 2; ++j) {
-            if (j < pairs && !(tagged(w[2 * j], epoch) && tagged(w[2 * j + 1], epoch))) {
-                const WordPair rr = poll_pair(slot + 2 * j, w[2 * j], w[2 * j + 1], epoch, p.timeout, misc, p.err);
-                if (!rr.ok) return;
-                w[2 * j] = rr.a;
-                w[2 * j + 1] = rr.b;
-            }
+            for (int m = 0; m < MPAD; ++m)
+                if (m < p.M) acc[m] += st[(j * p.M + m) * 32 + lane];
         }
-#pragma unroll
-        for (int m = 0; m < MPAD; ++m) sum[m] += __uint_as_float(static_cast<uint32_t>(w[m]));
+        __syncwarp();
     }
-    store_y<MPAD>(p, n, sum);
+    store_y<MPAD>(p, n, acc);
+    return true;
 }
 
 // Store one quantised slice (unit i, row m, 16-byte part l16) into the B
 // operand, the group scale into sXs, then arrive on unit i's barrier.
 template <int MPAD>
 __device__ __forceinline__ void put_slice(uint8_t* sB, float* sXs, uint64_t* bready, int i, int m, int l16,
-                                          uint32_t lo, uint32_t hi, float scale, bool with_scale) {
+                                          uint32_t lo, uint32_t hi, float scale) {
     uint8_t* row = sB + i * (MPAD * 128) + (m >> 3) * 1024 + (m & 7) * 128;
     *reinterpret_cast<uint2*>(row + (((l16 >> 1) ^ (m & 7)) << 4) + ((l16 & 1) << 3)) = make_uint2(lo, hi);
-    if (with_scale) sXs[i * MPAD + m] = scale;
+    if (l16 == 0) sXs[i * MPAD + m] = scale;
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(&bready[i]);
 }
@@ -311,19 +272,22 @@ __device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t
 }
 
 template <int MPAD, int KIND, bool DIST>
-__global__ void __launch_bounds__(kThreads, 1) fused_quant_gemm_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MPAD, DIST>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sW = smem + C::kOffW;
+    uint8_t* sRing = smem;
     uint8_t* sB = smem + C::kOffB;
     float* sXs = reinterpret_cast<float*>(smem + C::kOffXs);
     float* sWs = reinterpret_cast<float*>(smem + C::kOffWs);
     int* sKb = reinterpret_cast<int*>(smem + C::kOffKb);
     float2* sTab = reinterpret_cast<float2*>(smem + C::kOffTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t* accf = full + C::kUnits;
-    uint64_t* bready = accf + C::kUnits;
+    uint64_t* empty = full + S;
+    uint64_t* accf = empty + S;
+    uint64_t* acce = accf + kAccStages;
+    uint64_t* bready = acce + kAccStages;
     uint64_t* hdr_bar = bready + C::kUnits;  // completes once misc[kMiscHdrOk] is written
     volatile uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
 
@@ -334,21 +298,33 @@ __global__ void __launch_bounds__(kThreads, 1) fused_quant_gemm_kernel(const Par
     const uint32_t KB = static_cast<uint32_t>(p.KB);
     const uint32_t nt0 = u0 / KB, kb0 = u0 - nt0 * KB;
 
-    // ---- set-up: barriers, TMEM, scale table, per-unit K block and weight scale
+    // ---- set-up; the first ring tiles go out at once ---------------------------
     if (tid == 0) {
-        // arrivals per unit: one per 16-byte code slice, plus one per scale word
-        // when the activations come through the workspace
-        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (DIST ? 17 : 16);
-        for (int i = 0; i < cnt; ++i) {
-            ptx::mbar_init(&full[i], 1);
-            ptx::mbar_init(&accf[i], 1);
-            ptx::mbar_init(&bready[i], arrivals);
+        // arrivals per unit: one per 16-byte code slice (local quant) or one per
+        // copied group (exchange)
+        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (DIST ? 1 : 16);
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
         }
+        for (int a = 0; a < kAccStages; ++a) {
+            ptx::mbar_init(&accf[a], 1);
+            ptx::mbar_init(&acce[a], 4);
+        }
+        for (int i = 0; i < cnt; ++i) ptx::mbar_init(&bready[i], arrivals);
         ptx::mbar_init(hdr_bar, 1);
         misc[kMiscAbort] = 0;
         misc[kMiscHdrOk] = 0;
-        misc[kMiscIssued] = 0;
+        misc[kMiscCommitted] = 0;
         ptx::fence_mbar_init();
+        const uint64_t pol = ptx::policy_evict_first();
+        const int pre = cnt < S ? cnt : S;
+        for (int i = 0; i < pre; ++i) {
+            ptx::mbar_arrive_expect_tx(&full[i], kTileBytes);
+            ptx::bulk_g2s(sRing + i * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
+                          &full[i], pol);
+        }
+        misc[kMiscIssued] = static_cast<uint32_t>(pre);
     }
     if (warp == 1) {
         ptx::tmem_alloc(const_cast<uint32_t*>(&misc[kMiscTmem]), C::kTmemCols);
@@ -369,15 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_quant_gemm_kernel(const Par
     ptx::tc_fence_after();
     const uint32_t tmem = misc[kMiscTmem];
 
-    // ---- 1. weight stream: every tile of this CTA in flight at once ------------
-    if (tid == 0) {
-        const uint64_t pol = ptx::policy_evict_first();
-        for (int i = 0; i < cnt; ++i) {
-            ptx::mbar_arrive_expect_tx(&full[i], kTileBytes);
-            ptx::bulk_g2s(sW + i * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
-                          &full[i], pol);
-        }
-    }
     if (warp == 2 && lane == 0) {  // packed-weight header check
         const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->n == p.N && h->k == p.K &&
@@ -388,211 +355,202 @@ __global__ void __launch_bounds__(kThreads, 1) fused_quant_gemm_kernel(const Par
     // Everything below may read what the previous kernel on the stream wrote.
     if (p.pdl) ptx::griddep_wait();
     if (warp == 2 && lane == 0 && misc[kMiscHdrOk] == 0) record_error(p.err, FP8BS_ERR_SCALE_KIND);
+    const uint32_t epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
 
-    uint32_t epoch = 0;
-    if (!is_mma_warp(warp)) {
-        const int qt = quant_index(tid);
-        const int qw = qt >> 5;
-        const int l16 = qt & 15;
-        if constexpr (!DIST) {
-            // ---- 2. quantise this CTA's own units' groups ------------------------
-            // slice s = (unit i, row m, part l16), s = qt + kQuantThreads * j;
-            // all loads in flight first, then two slices at a time.
-            const int slices = cnt * p.M * 16;
-            uint4 raw[C::kSlices + 1];
+    if (warp == 0) {
+        // ---- 1. weight ring refills ------------------------------------------------
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_first();
+#pragma unroll 1
+            for (int i = S; i < cnt; ++i) {
+                const int s = i % S;
+                if (!wait_bar(&empty[s], static_cast<uint32_t>((i / S - 1) & 1), p, misc)) break;
+                ptx::mbar_arrive_expect_tx(&full[s], kTileBytes);
+                ptx::bulk_g2s(sRing + s * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
+                              &full[s], pol);
+                misc[kMiscIssued] = static_cast<uint32_t>(i + 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- 3. MMA issue --------------------------------------------------------------
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
+#pragma unroll 1
+            for (int i = 0; i < cnt; ++i) {
+                const int s = i % S, a = i % kAccStages;
+                if (!wait_bar(&bready[i], 0, p, misc)) break;
+                if (!wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc)) break;
+                if (i >= kAccStages && !wait_bar(&acce[a], static_cast<uint32_t>((i / kAccStages - 1) & 1), p, misc))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t wa = ptx::smem_addr(sRing + s * kTileBytes);
+                const uint32_t xb = ptx::smem_addr(sB + i * C::kBBytes);
 #pragma unroll
-            for (int j = 0; j < C::kSlices + 1; ++j) {
-                const int sl = qt + kQuantThreads * j;
+                for (int k = 0; k < 4; ++k)
+                    ptx::mma_f8f6f4(tmem + a * MPAD, ptx::smem_desc_sw128(wa + 32 * k),
+                                    ptx::smem_desc_sw128(xb + 32 * k), idesc, k > 0 ? 1u : 0u);
+                ptx::mma_commit(&empty[s]);
+                ptx::mma_commit(&accf[a]);
+                misc[kMiscCommitted] = static_cast<uint32_t>(i + 1);
+            }
+        }
+        __syncwarp();
+    } else {
+        const int qt = tid - 64;  // 0 .. kQuantThreads-1
+        const int hw = qt >> 4;
+        const int l16 = qt & 15;
+        const int hw_first = hw & ~1;  // the warp's first half-warp
+        if constexpr (!DIST) {
+            // ---- 2. quantise this CTA's own units' groups --------------------------
+            // group g = i * M + m (unit i, token m); half-warp hw takes g = hw + 12 j.
+            // All loads are in flight first; the rolled loop then quantises
+            // raw[0] and shifts the rest down, so its body appears once.
+            const int ngc = cnt * p.M;
+            uint4 raw[C::kGroupsPerHw];
+#pragma unroll
+            for (int j = 0; j < C::kGroupsPerHw; ++j) {
+                const int g = hw + kQuantHalfWarps * j;
                 raw[j] = make_uint4(0, 0, 0, 0);
-                if (j < C::kSlices && sl < slices) {
-                    const uint32_t g = static_cast<uint32_t>(sl) >> 4;
-                    const int i = static_cast<int>(div_m(g, p.mdiv));
-                    const int m = static_cast<int>(g) - i * p.M;
+                if (g < ngc) {
+                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(g), p.mdiv));
+                    const int m = g - i * p.M;
                     raw[j] = __ldg(reinterpret_cast<const uint4*>(p.x + m * p.ldx + sKb[i] * kTile + l16 * 8));
                 }
             }
-            epoch = ld_u32_gpu(p.gen + c) + 1;
-#pragma unroll
-            for (int j = 0; j < C::kSlices; j += 2) {
-                if (kQuantThreads * j + qw * 32 < slices) {  // warp-uniform: the reductions need all lanes
-                    const SliceQuant q0 = quant_slice<KIND>(raw[j], sTab);
-                    const SliceQuant q1 = quant_slice<KIND>(raw[j + 1], sTab);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int sl = qt + kQuantThreads * (j + h);
-                        const SliceQuant& qs = h == 0 ? q0 : q1;
-                        if (j + h < C::kSlices && sl < slices) {
-                            const uint32_t g = static_cast<uint32_t>(sl) >> 4;
-                            const int i = static_cast<int>(div_m(g, p.mdiv));
-                            const int m = static_cast<int>(g) - i * p.M;
-                            if (u0 + i < KB) put_xq_out<KIND>(p, m, sKb[i], l16, qs);  // n-tile 0 publishes xq / xs
-                            put_slice<MPAD>(sB, sXs, bready, i, m, l16, qs.lo, qs.hi, qs.scale, l16 == 0);
-                        }
-                    }
+#pragma unroll 1
+            for (int j = 0; hw_first + kQuantHalfWarps * j < ngc; ++j) {  // warp-uniform
+                const int g = hw + kQuantHalfWarps * j;
+                const SliceQuant qs = quant_slice<KIND>(raw[0], sTab);
+                if (g < ngc) {
+                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(g), p.mdiv));
+                    const int m = g - i * p.M;
+                    if (u0 + i < KB) put_xq_out<KIND>(p, m, sKb[i], l16, qs);  // n-tile 0 publishes xq / xs
+                    put_slice<MPAD>(sB, sXs, bready, i, m, l16, qs.lo, qs.hi, qs.scale);
                 }
+#pragma unroll
+                for (int t = 0; t + 1 < C::kGroupsPerHw; ++t) raw[t] = raw[t + 1];
             }
         } else {
-            // ---- 2a. this CTA's share of all groups: quantise, publish ----------
-            // group g = kb * M + m; half-warp h takes g0 + h, g0 + h + 12, ...
+            // ---- 2a. this CTA's share of all groups: quantise, publish ------------
+            // group g = kb * M + m; half-warp hw takes g0 + hw, g0 + hw + 12, ...
             const uint32_t NG = static_cast<uint32_t>(p.M) * KB;
             const uint32_t g0 = unit_begin(c, NG, G), g1 = unit_begin(c + 1, NG, G);
-            const int hw = qt >> 4;
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (g0 + hw < g1) {
-                const uint32_t g = g0 + hw;
-                const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
-                raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
-            }
-            epoch = ld_u32_gpu(p.gen + c) + 1;
-            for (uint32_t base = g0; base + qw * 2 < g1; base += kQuantHalfWarps) {  // warp-uniform
+#pragma unroll 1
+            for (uint32_t base = g0; base + hw_first < g1; base += kQuantHalfWarps) {  // warp-uniform
                 const uint32_t g = base + hw;
                 const bool valid = g < g1;
                 const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
-                if (base != g0 && valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
-                const SliceQuant qs = quant_slice<KIND>(valid ? raw : make_uint4(0, 0, 0, 0), sTab);
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
+                const SliceQuant qs = quant_slice<KIND>(raw, sTab);
                 if (valid) {
-                    const size_t row = static_cast<size_t>(kb) * 32 + m;
-                    st_pair(p.xqw + row * 32 + 2 * l16, tag(qs.lo, epoch), tag(qs.hi, epoch));
-                    const uint32_t sbits = KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale);
-                    if (l16 == 0) st_word(p.xsw + row, tag(sbits, epoch));
+                    *reinterpret_cast<uint2*>(kb_codes(p, kb) + m * 128 + l16 * 8) = make_uint2(qs.lo, qs.hi);
+                    if (l16 == 0)
+                        kb_scales(p, kb)[m] = KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale);
                     put_xq_out<KIND>(p, m, kb, l16, qs);
+                    __threadfence();
+                }
+                __syncwarp();
+                if (valid && l16 == 0) ptx::st_release_u32(kb_flags(p, kb) + m, epoch);
+            }
+            // ---- 2b. the groups of this CTA's units into shared memory -------------
+            // group gi = i * M + m; thread qt takes gi = qt + 192 j: wait for its
+            // flags, put all its copies in flight, then one wait.
+            const int ngc = cnt * p.M;
+            bool ok = true;
+#pragma unroll
+            for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                const int gi = qt + kQuantThreads * j;
+                if (ok && gi < ngc) {
+                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                    const int m = gi - i * p.M;
+                    ok = wait_flag(kb_flags(p, static_cast<uint32_t>(sKb[i])) + m, epoch, p, misc);
                 }
             }
-            // ---- 2b. the codes and scales of this CTA's units into shared memory
-            // code slice (unit i, row m, part l16); scale slice (unit i, row m):
-            // all loads in flight first, then each is re-read until it carries
-            // this call's epoch.
-            const int slices = cnt * p.M * 16;
-            const int sslices = cnt * p.M;
-            uint64_t w[C::kSlices][2];
+            if (ok) {
+                uint32_t sbits[C::kGroupsPerThread];
 #pragma unroll
-            for (int j = 0; j < C::kSlices; ++j) {
-                const int sl = qt + kQuantThreads * j;
-                w[j][0] = w[j][1] = 0;
-                if (sl < slices) {
-                    const uint32_t g = static_cast<uint32_t>(sl) >> 4;
-                    const int i = static_cast<int>(div_m(g, p.mdiv));
-                    const int m = static_cast<int>(g) - i * p.M;
-                    ld_pair(p.xqw + (static_cast<size_t>(sKb[i]) * 32 + m) * 32 + 2 * l16, w[j][0], w[j][1]);
-                }
-            }
-            uint64_t sw[C::kScaleSlices];
-#pragma unroll
-            for (int j = 0; j < C::kScaleSlices; ++j) {
-                const int sl = qt + kQuantThreads * j;
-                sw[j] = 0;
-                if (sl < sslices) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(sl), p.mdiv));
-                    const int m = sl - i * p.M;
-                    sw[j] = ld_word(p.xsw + static_cast<size_t>(sKb[i]) * 32 + m);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < C::kSlices; ++j) {
-                const int sl = qt + kQuantThreads * j;
-                if (sl < slices) {
-                    const uint32_t g = static_cast<uint32_t>(sl) >> 4;
-                    const int i = static_cast<int>(div_m(g, p.mdiv));
-                    const int m = static_cast<int>(g) - i * p.M;
-                    bool ok = true;
-                    if (!(tagged(w[j][0], epoch) && tagged(w[j][1], epoch))) {
-                        const uint64_t* src = p.xqw + (static_cast<size_t>(sKb[i]) * 32 + m) * 32 + 2 * l16;
-                        const WordPair r = poll_pair(src, w[j][0], w[j][1], epoch, p.timeout, misc, p.err);
-                        ok = r.ok;
-                        w[j][0] = r.a;
-                        w[j][1] = r.b;
+                for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                    const int gi = qt + kQuantThreads * j;
+                    sbits[j] = 0;
+                    if (gi < ngc) {
+                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                        const int m = gi - i * p.M;
+                        const uint32_t kb = static_cast<uint32_t>(sKb[i]);
+                        const uint8_t* src = kb_codes(p, kb) + m * 128;
+                        uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll 1
+                        for (int ch = 0; ch < 8; ++ch) ptx::cp_async16(row + ((ch ^ (m & 7)) << 4), src + ch * 16);
+                        sbits[j] = kb_scales(p, kb)[m];
                     }
-                    if (ok)
-                        put_slice<MPAD>(sB, sXs, bready, i, m, l16, static_cast<uint32_t>(w[j][0]),
-                                        static_cast<uint32_t>(w[j][1]), 0.0f, false);
                 }
-            }
+                ptx::cp_async_wait_all();
 #pragma unroll
-            for (int j = 0; j < C::kScaleSlices; ++j) {
-                const int sl = qt + kQuantThreads * j;
-                if (sl < sslices) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(sl), p.mdiv));
-                    const int m = sl - i * p.M;
-                    bool ok = true;
-                    if (!tagged(sw[j], epoch)) {
-                        const uint64_t* src = p.xsw + static_cast<size_t>(sKb[i]) * 32 + m;
-                        const WordPair r = poll_word(src, sw[j], epoch, p.timeout, misc, p.err);
-                        ok = r.ok;
-                        sw[j] = r.a;
-                    }
-                    if (ok) {
-                        const uint32_t bits = static_cast<uint32_t>(sw[j]);
-                        sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(bits) : __uint_as_float(bits);
+                for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                    const int gi = qt + kQuantThreads * j;
+                    if (gi < ngc) {
+                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                        const int m = gi - i * p.M;
+                        sXs[i * MPAD + m] =
+                            KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(sbits[j]) : __uint_as_float(sbits[j]);
+                        ptx::fence_proxy_async_smem();
                         ptx::mbar_arrive(&bready[i]);
                     }
                 }
             }
         }
-    } else {
-        epoch = ld_u32_gpu(p.gen + c) + 1;
-    }
 
-    if (is_mma_warp(warp)) {
-        // ---- 3. MMA issue: lane 0 of warp 1 takes the even units, of warp 3 the odd
-        if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
-            for (int i = warp == 1 ? 0 : 1; i < cnt; i += 2) {
-                if (!wait_phase(&bready[i], 0, p.timeout, misc, p.err, true)) break;
-                if (!wait_phase(&full[i], 0, p.timeout, misc, p.err, true)) break;
+        if (warp >= 4) {
+            // ---- 4./5. rescale-accumulate and output -------------------------------
+            const int q = warp & 3;
+            uint32_t hdr = 0;
+            if (lane == 0) hdr = wait_bar(hdr_bar, 0, p, misc) && misc[kMiscHdrOk] != 0;
+            const bool hdr_ok = __shfl_sync(0xFFFFFFFFu, hdr, 0) != 0;
+            float acc[MPAD];
+#pragma unroll
+            for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
+            uint32_t cur = nt0, kb = kb0;
+#pragma unroll 1
+            for (int i = 0; i < cnt; ++i) {
+                const int a = i % kAccStages;
+                uint32_t done = 0;
+                if (lane == 0)  // the MMA completion, and the operand barrier that published sXs[i]
+                    done = (wait_bar(&accf[a], static_cast<uint32_t>((i / kAccStages) & 1), p, misc) &&
+                            wait_bar(&bready[i], 0, p, misc)) ? 1u : 0u;
+                if (__shfl_sync(0xFFFFFFFFu, done, 0) == 0) break;
                 ptx::tc_fence_after();
-                const uint32_t a = ptx::smem_addr(sW + i * kTileBytes);
-                const uint32_t b = ptx::smem_addr(sB + i * C::kBBytes);
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
+                uint32_t r0[16], r1[16];
+                ptx::tmem_ld_32x32b_x16(taddr, r0);
+                if constexpr (MPAD == 32) ptx::tmem_ld_32x32b_x16(taddr + 16, r1);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&acce[a]);  // this warp is done with the stage
+                const float sw = sWs[i];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ptx::mma_f8f6f4(tmem + i * MPAD, ptx::smem_desc_sw128(a + 32 * k),
-                                    ptx::smem_desc_sw128(b + 32 * k), idesc, k > 0 ? 1u : 0u);
-                ptx::mma_commit(&accf[i]);
-                atomicOr(const_cast<uint32_t*>(&misc[kMiscIssued]), 1u << i);
-            }
-        }
-        __syncwarp();
-    } else if (warp >= 4) {
-        // ---- 4./5. rescale-accumulate and output ---------------------------------
-        const int q = warp & 3;
-        uint32_t hdr = 0;
-        if (lane == 0) hdr = wait_phase(hdr_bar, 0, p.timeout, misc, p.err, true) && misc[kMiscHdrOk] != 0;
-        const bool hdr_ok = __shfl_sync(0xFFFFFFFFu, hdr, 0) != 0;
-        float acc[MPAD];
+                for (int m = 0; m < 16; ++m) acc[m] = fmaf(__uint_as_float(r0[m]), sXs[i * MPAD + m] * sw, acc[m]);
+                if constexpr (MPAD == 32) {
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
-        uint32_t cur = nt0, kb = kb0;
-        for (int i = 0; i < cnt; ++i) {
-            uint32_t done = 0;
-            if (lane == 0)  // the MMA completion, and the operand barrier that published sXs[i]
-                done = (wait_phase(&accf[i], 0, p.timeout, misc, p.err, true) &&
-                        wait_phase(&bready[i], 0, p.timeout, misc, p.err, true)) ? 1u : 0u;
-            done = __shfl_sync(0xFFFFFFFFu, done, 0);
-            if (!done) break;
-            ptx::tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(i * MPAD);
-            uint32_t r0[16], r1[16];
-            ptx::tmem_ld_32x32b_x16(taddr, r0);
-            if constexpr (MPAD == 32) ptx::tmem_ld_32x32b_x16(taddr + 16, r1);
-            ptx::tmem_wait_ld();
-            const float sw = sWs[i];
+                    for (int m = 0; m < 16; ++m)
+                        acc[16 + m] = fmaf(__uint_as_float(r1[m]), sXs[i * MPAD + 16 + m] * sw, acc[16 + m]);
+                }
+                if (++kb == KB || i == cnt - 1) {  // the tile ends here, or this CTA's range does
+                    // whole tile in this CTA -> 0; this CTA started inside the tile
+                    // -> 1 (publish); the tile goes on in later CTAs -> 2 (reduce;
+                    // always this CTA's last unit, so the weight ring is idle)
+                    const bool starts_here = cur != nt0 || kb0 == 0;
+                    const bool ends_here = kb == KB;
+                    const int role = starts_here ? (ends_here ? 0 : 2) : 1;
+                    if (hdr_ok && !flush_tile<MPAD, C::kRingBytes / 16>(p, cur, acc, c, G, role, q, lane, epoch,
+                                                                         misc, reinterpret_cast<float*>(sRing)))
+                        break;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[m] = fmaf(__uint_as_float(r0[m]), sXs[i * MPAD + m] * sw, acc[m]);
-            if constexpr (MPAD == 32) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc[16 + m] = fmaf(__uint_as_float(r1[m]), sXs[i * MPAD + 16 + m] * sw, acc[16 + m]);
-            }
-            if (++kb == KB || i == cnt - 1) {  // the tile ends here, or this CTA's range does
-                // whole tile in this CTA -> 0; this CTA started inside the tile
-                // -> 1 (publish); the tile goes on in later CTAs -> 2 (reduce)
-                const bool starts_here = cur != nt0 || kb0 == 0;
-                const bool ends_here = kb == KB;
-                const int role = starts_here ? (ends_here ? 0 : 2) : 1;
-                if (hdr_ok) flush_tile<MPAD>(p, cur, acc, c, G, role, q, lane, epoch, misc);
-#pragma unroll
-                for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
-                ++cur;
-                kb = 0;
+                    for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
+                    ++cur;
+                    kb = 0;
+                }
             }
         }
     }
@@ -600,17 +558,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_quant_gemm_kernel(const Par
     // ---- teardown -------------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
-    if (misc[kMiscAbort] != 0) {
+    if (misc[kMiscAbort] != 0 && tid == 0) {
         // drain this CTA's own copies and MMAs before its shared memory and
         // TMEM go away (bounded as well)
-        if (tid == 0) {
-            for (int i = 0; i < cnt; ++i) wait_phase(&full[i], 0, p.timeout, misc, p.err, false);
-            const uint32_t issued = misc[kMiscIssued];
-            for (int i = 0; i < cnt; ++i)
-                if (issued & (1u << i)) wait_phase(&accf[i], 0, p.timeout, misc, p.err, false);
+        const int issued = static_cast<int>(misc[kMiscIssued]);
+        for (int s = 0; s < S && s < issued; ++s) {
+            const int uses = (issued - 1 - s) / S + 1;
+            drain_bar(&full[s], static_cast<uint32_t>((uses - 1) & 1), p.timeout);
         }
-        __syncthreads();
+        const int committed = static_cast<int>(misc[kMiscCommitted]);
+        if (committed > 0) {
+            const int j = committed - 1;
+            drain_bar(&accf[j % kAccStages], static_cast<uint32_t>((j / kAccStages) & 1), p.timeout);
+        }
     }
+    __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::kTmemCols);
@@ -624,7 +586,7 @@ template <int MPAD, int KIND, bool DIST>
 cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     using C = Cfg<MPAD, DIST>;
     auto kern = fused_quant_gemm_kernel<MPAD, KIND, DIST>;
-    // Opt in to the large dynamic shared memory once per device (not a stream
+    // Opt in to the dynamic shared memory once per device (not a stream
     // operation, so it is harmless during graph capture too).
     static int configured[64] = {0};
     int dev = 0;
@@ -650,8 +612,8 @@ cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
 
 template <int MPAD, int KIND, bool DIST>
 cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
-    // At most one CTA per SM, each with at most kUnits resident units: weights
-    // with more units than that go in several launches of whole n-tiles.
+    // At most one CTA per SM with at most kUnits units each: weights with more
+    // units than that go in several launches of whole n-tiles.
     const int KB = a.K / kTile, NT = a.N / kTile;
     const int cap_units = a.sm_count * Cfg<MPAD, DIST>::kUnits;
     const int chunk_nt = cap_units / KB;  // >= 1 (checked by the caller)
@@ -695,9 +657,9 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.ldy = a.ldy;
     p.err = reinterpret_cast<uint32_t*>(a.workspace);
     p.gen = reinterpret_cast<uint32_t*>(a.workspace + ws_gen_offset());
-    p.ll = reinterpret_cast<uint64_t*>(a.workspace + ws_partials_offset());
-    p.xsw = reinterpret_cast<uint64_t*>(a.workspace + ws_xs_offset(a.sm_count));
-    p.xqw = reinterpret_cast<uint64_t*>(a.workspace + ws_xq_offset(a.sm_count, a.K));
+    p.pflag = reinterpret_cast<uint32_t*>(a.workspace + ws_pflag_offset());
+    p.slots = reinterpret_cast<float*>(a.workspace + ws_partials_offset());
+    p.act = a.workspace + ws_act_offset(a.sm_count);
     p.timeout = a.timeout_cycles;
     p.pdl = a.pdl;
     if (a.kind == FP8BS_SCALE_UE8M0) return launch_kind<FP8BS_SCALE_UE8M0>(p, a, stream);

@@ -33,35 +33,41 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
     return kHeaderBytes + static_cast<size_t>(N / kTile) * static_cast<size_t>(K / kTile) * kTileBytes;
 }
 
-// Workspace layout (bytes).  Every word the fused GEMM exchanges through it is
-// 64 bits: 32 data bits and the 32-bit epoch of the call that wrote it, so
-// words left by earlier calls (of any shape) are never taken for this call's
-// and nothing has to be cleared between calls.
-//   [0, 256)                    device error word
-//   [256, 256 + 4 KB)           epoch words, one per possible CTA index
-//   then sm_count x 32 KB       split-K partial slots (128 rows x 32 columns)
-//   then K/128 x 256 B          activation scales   [K/128][32 rows]
-//   then K/128 x 8 KB           activation codes    [K/128][32 rows][32 words of 4 codes]
+// Workspace layout (bytes).  The CTAs of one fused launch exchange two kinds
+// of data through it: the quantised activations (each 1x128 group published
+// once, by one CTA) and the split-K partials.  Every published item has a
+// 32-bit flag that its writer sets to the call's epoch after the data, so
+// flags left by earlier calls carry older epochs and nothing is cleared
+// between calls.  Every region sits at a place that depends on sm_count only,
+// never on N or K, so a workspace serves calls of any shape without a flag of
+// one call ever landing on the data of another.
+//   [0, 256)                  device error word
+//   [256, +4 KB)              epoch words, one per possible CTA index
+//   [4352, +16 KB)            partial flags, one per (CTA index, epilogue warp)
+//   then sm_count x 16 KB     split-K partial slots, fp32 [32 columns][128 rows]
+//   then K/128 x 4352 B       one record per K block of the activations:
+//                             32 group flags, 32 scale words, 32 x 128 codes
 constexpr size_t kWsErrorBytes = 256;
-constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid (one CTA per SM)
+constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
 constexpr size_t kWsGenBytes = kMaxCtas * sizeof(uint32_t);
-constexpr size_t kSlotBytes = 128 * 32 * sizeof(uint64_t);
-constexpr size_t kXsRowBytes = 32 * sizeof(uint64_t);        // per K block
-constexpr size_t kXqRowBytes = 32 * 32 * sizeof(uint64_t);   // per K block
+constexpr size_t kWsPflagBytes = kMaxCtas * 4 * sizeof(uint32_t);
+constexpr size_t kSlotBytes = 32 * 128 * sizeof(float);
+constexpr size_t kKbRecFlags = 0;                   // within a K-block record
+constexpr size_t kKbRecScales = 32 * sizeof(uint32_t);
+constexpr size_t kKbRecCodes = 64 * sizeof(uint32_t);
+constexpr size_t kKbRecBytes = kKbRecCodes + 32 * 128;
 
-__host__ __device__ inline size_t ws_gen_offset() { return kWsErrorBytes; }
-__host__ __device__ inline size_t ws_partials_offset() { return kWsErrorBytes + kWsGenBytes; }
-__host__ __device__ inline size_t ws_xs_offset(int sm_count) {
+__host__ __device__ constexpr size_t ws_gen_offset() { return kWsErrorBytes; }
+__host__ __device__ constexpr size_t ws_pflag_offset() { return kWsErrorBytes + kWsGenBytes; }
+__host__ __device__ constexpr size_t ws_partials_offset() { return ws_pflag_offset() + kWsPflagBytes; }
+__host__ __device__ constexpr size_t ws_act_offset(int sm_count) {
     return ws_partials_offset() + static_cast<size_t>(sm_count) * kSlotBytes;
 }
-__host__ __device__ inline size_t ws_xq_offset(int sm_count, int64_t K) {
-    return ws_xs_offset(sm_count) + static_cast<size_t>(K / kTile) * kXsRowBytes;
-}
-__host__ __device__ inline size_t ws_total_bytes(int sm_count, int64_t K) {
-    return ws_xq_offset(sm_count, K) + static_cast<size_t>(K / kTile) * kXqRowBytes;
+__host__ __device__ constexpr size_t ws_total_bytes(int sm_count, int64_t K) {
+    return ws_act_offset(sm_count) + static_cast<size_t>(K / kTile) * kKbRecBytes;
 }
 
-// Units of work per CTA the fused kernel keeps resident in shared memory.
+// Units of work (128x128 weight tiles) one CTA of the fused kernel owns at most.
 constexpr int kMaxUnitsM16 = 12;
 constexpr int kMaxUnitsM32 = 10;
 

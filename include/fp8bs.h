@@ -163,11 +163,12 @@ enum {
 
 /* Workspace bytes the fused GEMM needs for an N x K weight on a device with
  * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
- * CUDA device): a 256-byte error word, 4 KB of epoch words, one 32 KB split-K
- * slot per multiprocessor and 8.25 KB per 128 columns of K for the quantised
- * activations the CTAs exchange.  The size depends on K and sm_count only and
- * every region sits at the same place for every N, so a workspace sized for
- * the largest K serves every weight of that K or less.  Returns 0 for an
+ * CUDA device): a 256-byte error word, 4 KB of epoch words, 16 KB of
+ * split-K flags, one 16 KB split-K slot per multiprocessor and 4.25 KB per 128
+ * columns of K for the quantised activations the CTAs exchange.  The size
+ * depends on K and sm_count only and every region sits at a place that
+ * depends on sm_count only, so a workspace sized for the largest K serves
+ * every weight of that K or less.  Returns 0 for an
  * unsupported shape (K/128 must not exceed 10 * sm_count). */
 size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count);
 
@@ -218,7 +219,7 @@ int fp8bs_check_error(void* workspace, void* stream);
 #define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */
 
 /* fp8bs_gemm_fused without a workspace argument: the scratch lives in one
- * fixed device array inside this library (6,328,576 bytes per device,
+ * fixed device array inside this library (3,199,232 bytes per device,
  * sized for FP8BS_STATIC_MAX_SMS CTAs and K up to FP8BS_STATIC_MAX_K), so the
  * call allocates no device memory, ever.  It is meant for callers that cannot
  * allocate or own device memory: an operator plugged into a runtime whose
@@ -239,8 +240,8 @@ int fp8bs_check_error(void* workspace, void* stream);
  *   cannot re-initialise the shared scratch, so after a timeout its epoch
  *   words may disagree and later calls may time out too.
  * Set-up: the first call on each device (with that device current) looks up
- * the array's address with cudaGetSymbolAddress, zeroes its error and epoch
- * words on `stream` and waits for that; make the first call before any stream
+ * the array's address with cudaGetSymbolAddress, zeroes it on `stream` and
+ * waits for that; make the first call before any stream
  * capture.
  * Sharing: every call on one device uses the same array, so two calls that
  * can overlap (different streams, different host threads without ordering)
