@@ -17,18 +17,21 @@
 // call's CTAs stream their weights while this call's CTAs finish.
 //   1. Weight ring: one thread keeps 4-5 tiles in flight with bulk async
 //      copies (TMA, evict-first), refilling a slot as soon as the MMAs that
-//      read it complete.  The first tiles go out at entry, before the wait for
-//      the previous kernel: they read only the packed weight.
+//      read it complete.  At entry, before the wait for the previous kernel
+//      (they read only the packed weight), the first tiles go to the ring and
+//      the rest of the CTA's tiles are prefetched into L2, so the whole weight
+//      stream starts at once and the refills hit L2.
 //   2. Activations into the shared-memory B operands (K-major, 128-byte
 //      swizzle), for all of the CTA's units:
-//        - up to 8 tokens every CTA quantises its own units' groups;
+//        - up to 6 tokens every CTA quantises its own units' groups;
 //        - above that each 1x128 group is quantised once, by one CTA, and
 //          published in the workspace (codes, scale, then a flag set to the
 //          call's epoch); a CTA copies the groups of its units with cp.async
 //          once their flags carry the epoch.
 //   3. One thread issues, per unit, four tcgen05.mma kind::f8f6f4 (K = 32
 //      each) with the weight tile as the 128-row A operand and the tokens as
-//      N = 16 or 32 ("swap-AB"), into one of 4 TMEM accumulator stages.
+//      N = 16 or 32 ("swap-AB"), into one of 4 TMEM accumulator stages, and
+//      one commit that both frees the ring slot and publishes the result.
 //   4. Four epilogue warps (one per 32 TMEM lanes) read each accumulator,
 //      free its stage, and accumulate P * (xs[m,kb] * ws[nt,kb]) in fp32
 //      registers (the per-K-block rescale of the page).
@@ -50,14 +53,15 @@
 namespace fp8bs {
 namespace {
 
-// 8 warps.  Warp 0: weight ring (one thread).  Warp 1: TMEM and MMA issue
-// (one thread).  Warp 2: unit info and header check, then quant.  Warp 3:
-// scale table, then quant.  Warps 4-7: quant, then the epilogue (one warp per
-// 32 TMEM lanes).
+// 8 warps.  Warp 0: weight ring (one thread).  Warps 1 and 3: MMA issue (one
+// thread each, even and odd units: one thread cannot keep the tensor pipe
+// fed); warp 1 also owns TMEM, warp 3 first builds the scale table.  Warp 2:
+// unit info and header check, then quant.  Warps 4-7: quant, then the
+// epilogue (one warp per 32 TMEM lanes).
 constexpr int kThreads = 256;
-constexpr int kQuantThreads = 192;  // warps 2-7
+constexpr int kQuantThreads = 160;  // warps 2 and 4-7
 constexpr int kQuantHalfWarps = kQuantThreads / 16;
-constexpr int kLocalMaxM = 8;  // up to this many tokens every CTA quantises its own groups
+constexpr int kLocalMaxM = 6;  // up to this many tokens every CTA quantises its own groups
 constexpr int kAccStages = 4;
 constexpr uint32_t kMaxSmemPerCta = 112 * 1024;  // two CTAs per SM
 
@@ -74,8 +78,8 @@ struct Cfg {
     static constexpr uint32_t kOffKb = kOffWs + kUnits * 4;
     static constexpr uint32_t kOffTab = (kOffKb + kUnits * 4 + 15) / 16 * 16;
     static constexpr uint32_t kOffBar = kOffTab + kScaleTab * 8;
-    // full[S], empty[S], accf[A], acce[A], bready[U], hdr
-    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAccStages + kUnits + 1;
+    // full[S], empty[S], acce[A], bready[U], hdr
+    static constexpr uint32_t kNumBars = 2 * kStages + kAccStages + kUnits + 1;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
     // local quant: groups (unit, token) per half-warp
@@ -109,6 +113,7 @@ struct Params {
     int pdl;
 };
 
+// kMiscCommitted + 0 / + 1: units committed by the even / odd MMA issuer
 enum : int { kMiscTmem = 0, kMiscAbort = 1, kMiscHdrOk = 2, kMiscIssued = 3, kMiscCommitted = 4 };
 
 __device__ __forceinline__ uint32_t unit_begin(uint32_t c, uint32_t T, uint32_t G) {
@@ -284,9 +289,8 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
     int* sKb = reinterpret_cast<int*>(smem + C::kOffKb);
     float2* sTab = reinterpret_cast<float2*>(smem + C::kOffTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t* empty = full + S;
-    uint64_t* accf = empty + S;
-    uint64_t* acce = accf + kAccStages;
+    uint64_t* empty = full + S;  // completes when the MMAs that read the slot are done
+    uint64_t* acce = empty + S;
     uint64_t* bready = acce + kAccStages;
     uint64_t* hdr_bar = bready + C::kUnits;  // completes once misc[kMiscHdrOk] is written
     volatile uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -307,15 +311,13 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < kAccStages; ++a) {
-            ptx::mbar_init(&accf[a], 1);
-            ptx::mbar_init(&acce[a], 4);
-        }
+        for (int a = 0; a < kAccStages; ++a) ptx::mbar_init(&acce[a], 4);
         for (int i = 0; i < cnt; ++i) ptx::mbar_init(&bready[i], arrivals);
         ptx::mbar_init(hdr_bar, 1);
         misc[kMiscAbort] = 0;
         misc[kMiscHdrOk] = 0;
         misc[kMiscCommitted] = 0;
+        misc[kMiscCommitted + 1] = 0;
         ptx::fence_mbar_init();
         const uint64_t pol = ptx::policy_evict_first();
         const int pre = cnt < S ? cnt : S;
@@ -325,6 +327,11 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                           &full[i], pol);
         }
         misc[kMiscIssued] = static_cast<uint32_t>(pre);
+        // the tiles that wait for a ring slot: start their HBM reads now, so
+        // the refills find them in L2 (they are contiguous: n-major units)
+        if (cnt > pre)
+            ptx::bulk_prefetch_l2(p.tiles + static_cast<size_t>(u0 + pre) * kTileBytes,
+                                  static_cast<uint32_t>(cnt - pre) * kTileBytes);
     }
     if (warp == 1) {
         ptx::tmem_alloc(const_cast<uint32_t*>(&misc[kMiscTmem]), C::kTmemCols);
@@ -352,10 +359,15 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
         misc[kMiscHdrOk] = ok ? 1u : 0u;
         ptx::mbar_arrive(hdr_bar);  // release: the epilogue reads the flag after waiting here
     }
+    // quantising threads: qt = 0 .. kQuantThreads-1 over warps 2, 4-7
+    const int qt = warp == 2 ? tid - 64 : tid - 96;
+    const int hw = qt >> 4;
+    const int l16 = qt & 15;
+    const int hw_first = hw & ~1;  // the warp's first half-warp
     // Everything below may read what the previous kernel on the stream wrote.
     if (p.pdl) ptx::griddep_wait();
     if (warp == 2 && lane == 0 && misc[kMiscHdrOk] == 0) record_error(p.err, FP8BS_ERR_SCALE_KIND);
-    const uint32_t epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
+    uint32_t epoch = 0;  // read by the quantising threads, after their x loads are in flight
 
     if (warp == 0) {
         // ---- 1. weight ring refills ------------------------------------------------
@@ -372,12 +384,13 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ---- 3. MMA issue --------------------------------------------------------------
+    } else if (warp == 1 || warp == 3) {
+        // ---- 3. MMA issue: warp 1 the even units, warp 3 the odd ones -------------
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
+            const int odd = warp == 3 ? 1 : 0;
 #pragma unroll 1
-            for (int i = 0; i < cnt; ++i) {
+            for (int i = odd; i < cnt; i += 2) {
                 const int s = i % S, a = i % kAccStages;
                 if (!wait_bar(&bready[i], 0, p, misc)) break;
                 if (!wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc)) break;
@@ -390,17 +403,12 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                 for (int k = 0; k < 4; ++k)
                     ptx::mma_f8f6f4(tmem + a * MPAD, ptx::smem_desc_sw128(wa + 32 * k),
                                     ptx::smem_desc_sw128(xb + 32 * k), idesc, k > 0 ? 1u : 0u);
-                ptx::mma_commit(&empty[s]);
-                ptx::mma_commit(&accf[a]);
-                misc[kMiscCommitted] = static_cast<uint32_t>(i + 1);
+                ptx::mma_commit(&empty[s]);  // frees the slot and publishes the accumulator
+                misc[kMiscCommitted + odd] = static_cast<uint32_t>(i + 1);
             }
         }
         __syncwarp();
     } else {
-        const int qt = tid - 64;  // 0 .. kQuantThreads-1
-        const int hw = qt >> 4;
-        const int l16 = qt & 15;
-        const int hw_first = hw & ~1;  // the warp's first half-warp
         if constexpr (!DIST) {
             // ---- 2. quantise this CTA's own units' groups --------------------------
             // group g = i * M + m (unit i, token m); half-warp hw takes g = hw + 12 j.
@@ -418,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                     raw[j] = __ldg(reinterpret_cast<const uint4*>(p.x + m * p.ldx + sKb[i] * kTile + l16 * 8));
                 }
             }
+            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
 #pragma unroll 1
             for (int j = 0; hw_first + kQuantHalfWarps * j < ngc; ++j) {  // warp-uniform
                 const int g = hw + kQuantHalfWarps * j;
@@ -436,13 +445,22 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
             // group g = kb * M + m; half-warp hw takes g0 + hw, g0 + hw + 12, ...
             const uint32_t NG = static_cast<uint32_t>(p.M) * KB;
             const uint32_t g0 = unit_begin(c, NG, G), g1 = unit_begin(c + 1, NG, G);
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (g0 + hw < g1) {
+                const uint32_t g = g0 + hw;
+                const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
+                raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
+            }
+            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
 #pragma unroll 1
             for (uint32_t base = g0; base + hw_first < g1; base += kQuantHalfWarps) {  // warp-uniform
                 const uint32_t g = base + hw;
                 const bool valid = g < g1;
                 const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
+                if (base != g0) {
+                    raw = make_uint4(0, 0, 0, 0);
+                    if (valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
+                }
                 const SliceQuant qs = quant_slice<KIND>(raw, sTab);
                 if (valid) {
                     *reinterpret_cast<uint2*>(kb_codes(p, kb) + m * 128 + l16 * 8) = make_uint2(qs.lo, qs.hi);
@@ -515,8 +533,11 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
             for (int i = 0; i < cnt; ++i) {
                 const int a = i % kAccStages;
                 uint32_t done = 0;
-                if (lane == 0)  // the MMA completion, and the operand barrier that published sXs[i]
-                    done = (wait_bar(&accf[a], static_cast<uint32_t>((i / kAccStages) & 1), p, misc) &&
+                // the MMA completion (the slot's release: its phase cannot move on
+                // before every epilogue warp has freed this unit's TMEM stage), and
+                // the operand barrier that published sXs[i]
+                if (lane == 0)
+                    done = (wait_bar(&empty[i % S], static_cast<uint32_t>((i / S) & 1), p, misc) &&
                             wait_bar(&bready[i], 0, p, misc)) ? 1u : 0u;
                 if (__shfl_sync(0xFFFFFFFFu, done, 0) == 0) break;
                 ptx::tc_fence_after();
@@ -566,10 +587,12 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
             const int uses = (issued - 1 - s) / S + 1;
             drain_bar(&full[s], static_cast<uint32_t>((uses - 1) & 1), p.timeout);
         }
-        const int committed = static_cast<int>(misc[kMiscCommitted]);
-        if (committed > 0) {
-            const int j = committed - 1;
-            drain_bar(&accf[j % kAccStages], static_cast<uint32_t>((j / kAccStages) & 1), p.timeout);
+        for (int odd = 0; odd < 2; ++odd) {
+            const int committed = static_cast<int>(misc[kMiscCommitted + odd]);
+            if (committed > 0) {  // the issuer's last commit covers all of its MMAs
+                const int j = committed - 1;
+                drain_bar(&empty[j % S], static_cast<uint32_t>((j / S) & 1), p.timeout);
+            }
         }
     }
     __syncthreads();

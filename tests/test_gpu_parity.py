@@ -206,7 +206,7 @@ def test_prepack_layout(dev, kind):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("kind", [F32, UE8])
-@pytest.mark.parametrize("M", [1, 5, 16, 17, 32])
+@pytest.mark.parametrize("M", [1, 5, 6, 7, 16, 17, 32])
 @pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 640), (1024, 1024), (640, 2048)])
 def test_fused_small_shapes(dev, oracle_mod, kind, M, N, K):
     run_fused(oracle_mod, dev, M, N, K, kind, seed=M * 131 + N + K)
