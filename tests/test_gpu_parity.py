@@ -212,6 +212,20 @@ def test_fused_small_shapes(dev, oracle_mod, kind, M, N, K):
     run_fused(oracle_mod, dev, M, N, K, kind, seed=M * 131 + N + K)
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8])
+@pytest.mark.parametrize("N,K,kind", [(128, 128, F32), (384, 640, F32), (640, 2048, UE8), (5120, 4096, F32),
+                                      (4608, 4096, F32), (4096, 2048, F32), (7168, 2048, UE8),
+                                      (1536, 7168, UE8), (4096, 4096, UE8)])
+def test_fused_few_tokens(dev, oracle_mod, N, K, kind, M):
+    # the local-quant variant (up to 6 tokens) and the exchange variant (7, 8)
+    # on every benchmark shape and a few small ones, quant bytes included
+    run_fused(oracle_mod, dev, M, N, K, kind, seed=5000 + 7 * M + N // 128 + K // 128)
+
+
+def test_fused_few_tokens_strided(dev, oracle_mod):
+    run_fused(oracle_mod, dev, 3, 1024, 1024, F32, seed=9, ldx_pad=64, ldy_pad=8)
+
+
 @pytest.mark.parametrize("M", [1, 3, 4, 8, 9, 16, 17, 24, 32])
 def test_fused_m_sweep_5120x4096(dev, oracle_mod, M):
     # the M sweep at N=5120, K=4096 with bit-exact quant bytes and scales
