@@ -313,7 +313,7 @@ class Step:
     """Packed weights, activations and the CUDA graph of one step."""
 
     def __init__(self, fb, torch, calls, dev, stream, io: bool = False, graph: bool = True,
-                 pdl: bool = True):
+                 pdl: bool = True, two_launch: bool = False):
         import synth
         self.calls = calls
         self.packs = {}
@@ -338,6 +338,14 @@ class Step:
                   for (M, N, K, _k, _w) in calls}
         self.io = io
         self.pdl = pdl
+        # the two-launch path: fp8bs_quant, then fp8bs_gemm_prequant on its output
+        self.two_launch = two_launch
+        if two_launch:
+            self.xq = {(M, K): torch.empty((M, K), dtype=torch.uint8, device=dev)
+                       for (M, N, K, _k, _w) in calls}
+            self.xs = {(M, K, kind): torch.empty((M, K // 128), device=dev,
+                                                 dtype=torch.uint8 if kind == 1 else torch.float32)
+                       for (M, N, K, kind, _w) in calls}
         if io:
             self.x_host = [torch.empty((c[0], c[2]), dtype=torch.bfloat16).pin_memory()
                            for c in calls]
@@ -374,8 +382,14 @@ class Step:
             y = self.y[(M, N)]
             if self.io:
                 x.copy_(self.x_host[i], non_blocking=True)
-            self.fb.fp8bs_gemm_fused(x, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
-                                     workspace=self.workspace, pdl=self.pdl, stream=self.stream)
+            if self.two_launch:
+                xq, xs = self.xq[(M, K)], self.xs[(M, K, kind)]
+                self.fb.fp8bs_quant(x, kind, xq=xq, xs=xs, stream=self.stream)
+                self.fb.fp8bs_gemm_prequant(xq, xs, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
+                                            workspace=self.workspace, stream=self.stream)
+            else:
+                self.fb.fp8bs_gemm_fused(x, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
+                                         workspace=self.workspace, pdl=self.pdl, stream=self.stream)
             if self.io:
                 self.y_host[i].copy_(y, non_blocking=True)
 
@@ -398,11 +412,13 @@ def time_steps(torch, step: Step, steps: int, warmup: int, world: int, dev) -> f
     return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
 
-def per_m_table(fb, torch, dev, stream, pdl):
-    """us/call and GB/s per M at N=5120 K=4096 (graph of 24 rotated calls)."""
+def per_m_table(fb, torch, dev, stream, pdl, two_launch=False):
+    """us/call and GB/s per M at N=5120 K=4096 (graph of 24 rotated calls);
+    two_launch: fp8bs_quant + fp8bs_gemm_prequant per call instead."""
     out = {}
     for M in M_SWEEP:
-        st = Step(fb, torch, [(M, 5120, 4096, 0, c) for c in range(COPIES)], dev, stream, pdl=pdl)
+        st = Step(fb, torch, [(M, 5120, 4096, 0, c) for c in range(COPIES)], dev, stream, pdl=pdl,
+                  two_launch=two_launch)
         progress(f"per-M step M={M}")
         reps = 50
         ms = time_steps(torch, st, reps, 5, 1, dev)
@@ -466,10 +482,12 @@ def run_gpu(args):
     del st_io
     torch.cuda.empty_cache()
 
-    per_m = None
+    per_m = per_m_two = None
     if args.workload == "msweep" and rank == 0 and not args.no_per_m:
         progress("per-M table")
         per_m = per_m_table(fb, torch, dev, stream, pdl)
+        progress("per-M table, two-launch path")
+        per_m_two = per_m_table(fb, torch, dev, stream, pdl, two_launch=True)
 
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -494,6 +512,7 @@ def run_gpu(args):
                                  else "one CUDA graph replay per step"),
                        "pdl": pdl},
             "per_m_us_and_GBps": per_m,
+            "per_m_two_launch_us_and_GBps": per_m_two,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),
                          "peak_source": peak_src, "kernel": "fused_quant_gemm_kernel",

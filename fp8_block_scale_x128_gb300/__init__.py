@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
             "fp8bs_gemm_fused": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, sz, vp, vp,
                                   c.c_uint, vp], ci),
             "fp8bs_check_error": ([vp, vp], ci),
+            "fp8bs_gemm_prequant": ([vp, i64, i64, vp, vp, sz, i64, i64, ci, vp, i64, vp, sz, c.c_uint, vp],
+                                    ci),
             "fp8bs_gemm_fused_static": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, vp, vp,
                                          c.c_uint, vp], ci),
         }
@@ -249,6 +251,29 @@ def fp8bs_gemm_fused(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
         y.stride(0), _ptr(workspace), workspace.numel(), _ptr(xq_out), _ptr(xs_out),
         FP8BS_FLAG_PDL if pdl else 0, _stream(stream))
     _check(rc, "fp8bs_gemm_fused")
+    return y
+
+
+def fp8bs_gemm_prequant(xq: torch.Tensor, xs: torch.Tensor, packed: torch.Tensor, N: int, K: int,
+                        scale_kind: int = FP8BS_SCALE_F32, y: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, pdl: bool = False,
+                        stream=None) -> torch.Tensor:
+    """Y = bf16(xq . W^T) with the block scales, for pre-quantised activations
+    (uint8 e4m3 codes [M, K], scales [M, K/128] fp32 or uint8 e8m0): the
+    second launch of the two-launch path."""
+    _require_cuda(xq, xs, packed, y, workspace)
+    assert xq.dtype == torch.uint8 and xq.dim() == 2 and xq.stride(1) == 1 and xq.shape[1] == K
+    assert xs.is_contiguous() and xs.shape == (xq.shape[0], K // 128)
+    M = xq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    if workspace is None:
+        workspace = new_workspace(N, K, xq.device, stream)
+    rc = lib().fp8bs_gemm_prequant(
+        _ptr(xq), M, xq.stride(0), _ptr(xs), _ptr(packed), packed.numel(), N, K, int(scale_kind),
+        _ptr(y), y.stride(0), _ptr(workspace), workspace.numel(), FP8BS_FLAG_PDL if pdl else 0,
+        _stream(stream))
+    _check(rc, "fp8bs_gemm_prequant")
     return y
 
 

@@ -210,6 +210,45 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     return status_of(launch_fused(a, as_stream(stream)));
 }
 
+int fp8bs_gemm_prequant(const uint8_t* xq, int64_t M, int64_t ldxq, const void* xs, const void* packed,
+                        size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y, int64_t ldy,
+                        void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+    if (!kind_ok(scale_kind) || (flags & ~static_cast<unsigned>(FP8BS_FLAG_PDL)) != 0) return FP8BS_ERR_ARG;
+    if (M < 0 || M > FP8BS_MAX_M || !nk_ok(N, K)) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!xq || !xs || !packed || !y || !workspace) return FP8BS_ERR_ARG;
+    if (ldxq < K || ldy < N) return FP8BS_ERR_ARG;
+    if (!aligned(xq, 16) || ldxq % 16 != 0 || !aligned(y, 16) || ldy % 8 != 0 || !aligned(packed, 256) ||
+        !aligned(workspace, 256) || (scale_kind == FP8BS_SCALE_F32 && !aligned(xs, 4)))
+        return FP8BS_ERR_ALIGN;
+    if (packed_bytes < fp8bs_packed_weight_bytes(N, K, scale_kind)) return FP8BS_ERR_WORKSPACE;
+    int sm = 0;
+    const int rc = current_sm_count(&sm);
+    if (rc != FP8BS_OK) return rc;
+    if (!fused_shape_supported(N, K, sm)) return FP8BS_ERR_SHAPE;
+    if (workspace_bytes < workspace_bytes_for(K, sm)) return FP8BS_ERR_WORKSPACE;
+    FusedArgs a;
+    a.x = nullptr;
+    a.ldx = 0;
+    a.packed = static_cast<const uint8_t*>(packed);
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.kind = scale_kind;
+    a.y = y;
+    a.ldy = ldy;
+    a.workspace = static_cast<uint8_t*>(workspace);
+    a.xq_out = nullptr;
+    a.xs_out = nullptr;
+    a.sm_count = sm;
+    a.timeout_cycles = kDefaultTimeoutCycles;
+    a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
+    a.xq_in = xq;
+    a.ldxq = ldxq;
+    a.xs_in = xs;
+    return status_of(launch_fused(a, as_stream(stream)));
+}
+
 int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
                             size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
                             int64_t ldy, uint8_t* xq_out, void* xs_out, uint32_t* status_out,

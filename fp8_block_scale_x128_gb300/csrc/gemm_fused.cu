@@ -65,7 +65,14 @@ constexpr int kLocalMaxM = 6;  // up to this many tokens every CTA quantises its
 constexpr int kAccStages = 4;
 constexpr uint32_t kMaxSmemPerCta = 112 * 1024;  // two CTAs per SM
 
-template <int MPAD, bool DIST>
+// Where a CTA's activation codes come from.
+enum : int {
+    kSrcLocal = 0,     // every CTA quantises its own units' groups (few tokens)
+    kSrcExchange = 1,  // each group quantised once, exchanged through the workspace
+    kSrcInput = 2,     // codes and scales given by the caller (the two-launch path)
+};
+
+template <int MPAD, int SRC>
 struct Cfg {
     static constexpr int kUnits = MPAD == 16 ? kMaxUnitsM16 : kMaxUnitsM32;
     static constexpr int kStages = MPAD == 16 ? 5 : 4;
@@ -109,6 +116,9 @@ struct Params {
     uint8_t* act;             // activation records [K/128][kKbRecBytes]
     uint8_t* xq_out;
     void* xs_out;
+    const uint8_t* xq_in;     // kSrcInput: codes [M][ldxq], scales [M][K/128]
+    int64_t ldxq;
+    const void* xs_in;
     long long timeout;
     int pdl;
 };
@@ -276,9 +286,9 @@ __device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t
     }
 }
 
-template <int MPAD, int KIND, bool DIST>
+template <int MPAD, int KIND, int SRC>
 __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __grid_constant__ Params p) {
-    using C = Cfg<MPAD, DIST>;
+    using C = Cfg<MPAD, SRC>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -306,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
     if (tid == 0) {
         // arrivals per unit: one per 16-byte code slice (local quant) or one per
         // copied group (exchange)
-        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (DIST ? 1 : 16);
+        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (SRC == kSrcLocal ? 16 : 1);
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
@@ -409,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
         }
         __syncwarp();
     } else {
-        if constexpr (!DIST) {
+        if constexpr (SRC == kSrcLocal) {
             // ---- 2. quantise this CTA's own units' groups --------------------------
             // group g = i * M + m (unit i, token m); half-warp hw takes g = hw + 12 j.
             // All loads are in flight first; the rolled loop then quantises
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
 #pragma unroll
                 for (int t = 0; t + 1 < C::kGroupsPerHw; ++t) raw[t] = raw[t + 1];
             }
-        } else {
+        } else if constexpr (SRC == kSrcExchange) {
             // ---- 2a. this CTA's share of all groups: quantise, publish ------------
             // group g = kb * M + m; half-warp hw takes g0 + hw, g0 + hw + 12, ...
             const uint32_t NG = static_cast<uint32_t>(p.M) * KB;
@@ -515,6 +525,41 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                         ptx::fence_proxy_async_smem();
                         ptx::mbar_arrive(&bready[i]);
                     }
+                }
+            }
+        } else {
+            // ---- 2. the caller's codes and scales of this CTA's units --------------
+            // group gi = i * M + m; thread qt takes gi = qt + 160 j: all copies in
+            // flight, then one wait.
+            const int ngc = cnt * p.M;
+            uint32_t sbits[C::kGroupsPerThread];
+#pragma unroll
+            for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                const int gi = qt + kQuantThreads * j;
+                sbits[j] = 0;
+                if (gi < ngc) {
+                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                    const int m = gi - i * p.M;
+                    const int kb = sKb[i];
+                    const uint8_t* src = p.xq_in + m * p.ldxq + kb * kTile;
+                    uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll 1
+                    for (int ch = 0; ch < 8; ++ch) ptx::cp_async16(row + ((ch ^ (m & 7)) << 4), src + ch * 16);
+                    sbits[j] = KIND == FP8BS_SCALE_UE8M0 ? static_cast<const uint8_t*>(p.xs_in)[m * p.KB + kb]
+                                                         : static_cast<const uint32_t*>(p.xs_in)[m * p.KB + kb];
+                }
+            }
+            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
+            ptx::cp_async_wait_all();
+#pragma unroll
+            for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                const int gi = qt + kQuantThreads * j;
+                if (gi < ngc) {
+                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                    const int m = gi - i * p.M;
+                    sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(sbits[j]) : __uint_as_float(sbits[j]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive(&bready[i]);
                 }
             }
         }
@@ -605,10 +650,10 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
         for (uint32_t j = c + lane * G; j < static_cast<uint32_t>(kMaxCtas); j += 32 * G) p.gen[j] = epoch;
 }
 
-template <int MPAD, int KIND, bool DIST>
+template <int MPAD, int KIND, int SRC>
 cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
-    using C = Cfg<MPAD, DIST>;
-    auto kern = fused_quant_gemm_kernel<MPAD, KIND, DIST>;
+    using C = Cfg<MPAD, SRC>;
+    auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC>;
     // Opt in to the dynamic shared memory once per device (not a stream
     // operation, so it is harmless during graph capture too).
     static int configured[64] = {0};
@@ -633,12 +678,12 @@ cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int MPAD, int KIND, bool DIST>
+template <int MPAD, int KIND, int SRC>
 cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
     // At most one CTA per SM with at most kUnits units each: weights with more
     // units than that go in several launches of whole n-tiles.
     const int KB = a.K / kTile, NT = a.N / kTile;
-    const int cap_units = a.sm_count * Cfg<MPAD, DIST>::kUnits;
+    const int cap_units = a.sm_count * Cfg<MPAD, SRC>::kUnits;
     const int chunk_nt = cap_units / KB;  // >= 1 (checked by the caller)
     const size_t scale_bytes = a.kind == FP8BS_SCALE_UE8M0 ? 1 : 4;
     for (int nt_base = 0; nt_base < NT; nt_base += chunk_nt) {
@@ -651,7 +696,7 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
         p.xs_out = nt_base == 0 ? a.xs_out : nullptr;
         p.pdl = nt_base == 0 ? a.pdl : 1;  // later chunks follow our own launch, which never writes packed
         const int grid = static_cast<int>(p.T) < a.sm_count ? static_cast<int>(p.T) : a.sm_count;
-        const cudaError_t e = launch_impl<MPAD, KIND, DIST>(p, grid, stream);
+        const cudaError_t e = launch_impl<MPAD, KIND, SRC>(p, grid, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -659,9 +704,13 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
 
 template <int KIND>
 cudaError_t launch_kind(const Params& p, const FusedArgs& a, cudaStream_t stream) {
-    if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, false>(p, a, stream);
-    if (a.M <= 16) return launch_chunks<16, KIND, true>(p, a, stream);
-    return launch_chunks<32, KIND, true>(p, a, stream);
+    if (a.xq_in) {
+        if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput>(p, a, stream);
+        return launch_chunks<32, KIND, kSrcInput>(p, a, stream);
+    }
+    if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, kSrcLocal>(p, a, stream);
+    if (a.M <= 16) return launch_chunks<16, KIND, kSrcExchange>(p, a, stream);
+    return launch_chunks<32, KIND, kSrcExchange>(p, a, stream);
 }
 
 }  // namespace
@@ -683,6 +732,9 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.pflag = reinterpret_cast<uint32_t*>(a.workspace + ws_pflag_offset());
     p.slots = reinterpret_cast<float*>(a.workspace + ws_partials_offset());
     p.act = a.workspace + ws_act_offset(a.sm_count);
+    p.xq_in = a.xq_in;
+    p.ldxq = a.ldxq;
+    p.xs_in = a.xs_in;
     p.timeout = a.timeout_cycles;
     p.pdl = a.pdl;
     if (a.kind == FP8BS_SCALE_UE8M0) return launch_kind<FP8BS_SCALE_UE8M0>(p, a, stream);

@@ -270,6 +270,10 @@ struct FusedArgs {
     int sm_count;
     long long timeout_cycles;
     int pdl;
+    // the two-launch path: pre-quantised activations instead of x (x unused)
+    const uint8_t* xq_in = nullptr;  // [M][ldxq] e4m3 codes
+    int64_t ldxq = 0;
+    const void* xs_in = nullptr;     // [M][K/128] fp32 or e8m0 scales
 };
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream);

@@ -208,6 +208,23 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
                      int64_t ldy, void* workspace, size_t workspace_bytes, uint8_t* xq_out,
                      void* xs_out, unsigned flags, void* stream);
 
+/* The GEMM on activations quantised beforehand: the second launch of the
+ * two-launch path ([P1] "Motivation": the per-1x128 quant and the block-scale
+ * GEMM as separate kernels, the path the fused call replaces; "Kernel
+ * microbenchmarks" times the two against it).  fp8bs_quant followed by this
+ * call gives a Y bit-identical to fp8bs_gemm_fused on the same x: the MMAs,
+ * the rescale and the split-K order are the same.
+ *   xq   : e4m3fn codes [M, K], row stride ldxq (xq and ldxq 16-byte aligned).
+ *   xs   : [M, K/128] scales, fp32 (4-byte aligned) or e8m0 bytes, of the
+ *          kind scale_kind (the packed weight's kind).
+ * Everything else as fp8bs_gemm_fused (flags: 0 or FP8BS_FLAG_PDL).
+ * Errors (host): ARG, SHAPE, ALIGN, WORKSPACE, CUDA.  Errors (device, via
+ * fp8bs_check_error): SCALE_KIND, TIMEOUT. */
+int fp8bs_gemm_prequant(const uint8_t* xq, int64_t M, int64_t ldxq, const void* xs, const void* packed,
+                        size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
+                        int64_t ldy, void* workspace, size_t workspace_bytes, unsigned flags,
+                        void* stream);
+
 /* Synchronise `stream`, read the workspace error word, clear it, and return
  * FP8BS_OK or the first device-side status recorded since the last check.
  * After FP8BS_ERR_TIMEOUT the epoch words may disagree: call

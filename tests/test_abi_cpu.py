@@ -130,6 +130,35 @@ def test_gemm_fused_static_empty_batch_is_a_no_op(L):
     assert gemm_static(L, M=0, x=None, y=None) == OK
 
 
+def gemm_prequant(L, xq=P, M=4, ldxq=4096, xs=P, packed=P, packed_bytes=1 << 30, N=5120, K=4096, kind=0,
+                  y=P, ldy=5120, ws=P, ws_bytes=1 << 30, flags=0):
+    return L.fp8bs_gemm_prequant(xq, M, ldxq, xs, packed, packed_bytes, N, K, kind, y, ldy, ws, ws_bytes,
+                                 flags, STREAM)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=3), ARG),
+    (dict(flags=2), ARG),
+    (dict(M=33), SHAPE),
+    (dict(K=4000, ldxq=4000), SHAPE),
+    (dict(xq=None), ARG),
+    (dict(xs=None), ARG),
+    (dict(ws=None), ARG),
+    (dict(ldxq=4080), ARG),
+    (dict(xq=P + 8), ALIGN),
+    (dict(ldxq=4104), ALIGN),
+    (dict(xs=P + 2), ALIGN),
+    (dict(y=P + 2), ALIGN),
+    (dict(packed_bytes=1000), WS),
+])
+def test_gemm_prequant_host_checks(L, kw, status):
+    assert gemm_prequant(L, **kw) == status
+
+
+def test_gemm_prequant_empty_batch_is_a_no_op(L):
+    assert gemm_prequant(L, M=0, xq=None, xs=None, y=None) == OK
+
+
 def test_quant_host_checks(L):
     q = L.fp8bs_quant
     assert q(P, 2, 4096, 4096, 3, P, P, STREAM) == ARG

@@ -255,6 +255,55 @@ def test_fused_weight_larger_than_one_launch(dev, oracle_mod, M, kind):
     run_fused(oracle_mod, dev, M, 16384, 8192, kind, seed=4000 + M, want_quant=False)
 
 
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 384, 640), (9, 1024, 1024), (17, 640, 2048),
+                                   (32, 5120, 4096), (3, 5120, 4096), (16, 4096, 2048)])
+def test_prequant_gemm_against_oracle(dev, oracle_mod, kind, M, N, K):
+    # the second launch of the two-launch path, fed the oracle's quantised x
+    x = synth.x_bf16(M, K, seed=6000 + M + K // 128)
+    xq_ref, xs_ref = oracle_mod.quant_1x128(x, kind)
+    wq, ws = H.weight(oracle_mod, N, K, kind, seed=6001 + N // 128)
+    y_ref = oracle_mod.gemm(xq_ref, xs_ref, wq, ws, kind, nthreads=H.threads())
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind)
+    xs_d = to_dev(xs_ref, dev) if kind == UE8 else to_dev(xs_ref, dev)
+    wsp = fb.new_workspace(N, K, dev)
+    y = fb.fp8bs_gemm_prequant(to_dev(xq_ref, dev), xs_d, packed, N, K, kind, workspace=wsp)
+    assert fb.fp8bs_check_error(wsp) == 0
+    H.check_y(H.torch_u16_to_np(y), y_ref, f"prequant M={M} N={N} K={K} kind={kind}")
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("M", [1, 6, 7, 16, 17, 32])
+def test_two_launch_path_is_bit_identical_to_fused(dev, kind, M):
+    # fp8bs_quant + fp8bs_gemm_prequant runs the same MMAs, rescale and split-K
+    # order as the fused call on the same x
+    N, K = 5120, 4096
+    x = synth.x_bf16_torch(M, K, seed=77 + M, device=dev)
+    w = synth.w_f32_torch(N, K, seed=78, device=dev)
+    wq, ws = fb.fp8bs_quant_weight(w, kind)
+    packed = fb.fp8bs_prepack_weight(wq, ws, kind)
+    wsp = fb.new_workspace(N, K, dev)
+    y_fused = fb.fp8bs_gemm_fused(x, packed, N, K, kind, workspace=wsp)
+    xq, xs = fb.fp8bs_quant(x, kind)
+    y_two = fb.fp8bs_gemm_prequant(xq, xs, packed, N, K, kind, workspace=wsp)
+    assert fb.fp8bs_check_error(wsp) == 0
+    assert torch.equal(y_fused.view(torch.int16), y_two.view(torch.int16))
+
+
+def test_prequant_strided_codes(dev, oracle_mod):
+    M, N, K = 7, 1024, 2048
+    x = synth.x_bf16(M, K, seed=41)
+    xq_ref, xs_ref = oracle_mod.quant_1x128(x, F32)
+    wq, ws = H.weight(oracle_mod, N, K, F32, seed=42)
+    y_ref = oracle_mod.gemm(xq_ref, xs_ref, wq, ws, F32, nthreads=H.threads())
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), F32)
+    xq_full = torch.zeros((M, K + 48), dtype=torch.uint8, device=dev)
+    xq_full[:, :K] = to_dev(xq_ref, dev)
+    y = fb.fp8bs_gemm_prequant(xq_full[:, :K], to_dev(xs_ref, dev), packed, N, K, F32)
+    torch.cuda.synchronize()
+    H.check_y(H.torch_u16_to_np(y), y_ref, "prequant strided")
+
+
 def test_fused_strided_x_and_y(dev, oracle_mod):
     run_fused(oracle_mod, dev, 7, 640, 1024, F32, seed=11, ldx_pad=64, ldy_pad=24)
 
