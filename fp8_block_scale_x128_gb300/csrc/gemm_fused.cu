@@ -25,13 +25,19 @@
 //      swizzle), for all of the CTA's units:
 //        - up to 6 tokens every CTA quantises its own units' groups;
 //        - above that each 1x128 group is quantised once, by one CTA, and
-//          published in the workspace (codes, scale, then a flag set to the
-//          call's epoch); a CTA copies the groups of its units with cp.async
-//          once their flags carry the epoch.
-//   3. One thread issues, per unit, four tcgen05.mma kind::f8f6f4 (K = 32
-//      each) with the weight tile as the 128-row A operand and the tokens as
-//      N = 16 or 32 ("swap-AB"), into one of 4 TMEM accumulator stages, and
-//      one commit that both frees the ring slot and publishes the result.
+//          published in the workspace as 64-bit words that each carry 32 bits
+//          of data (4 codes or the scale) and the call's epoch, with no fence
+//          or flag; a CTA reads the words of its units' groups, re-reads the
+//          ones that still carry an older epoch, and stores the codes into
+//          its operands (a 64-bit access is single-copy atomic, so a word is
+//          either old or wholly new);
+//        - with caller-quantised input the codes and scales are copied with
+//          cp.async.
+//   3. Two threads (even and odd units) issue, per unit, four tcgen05.mma
+//      kind::f8f6f4 (K = 32 each) with the weight tile as the 128-row A
+//      operand and the tokens as N = 16 or 32 ("swap-AB"), into one of 4 TMEM
+//      accumulator stages, and one commit that both frees the ring slot and
+//      publishes the result.
 //   4. Four epilogue warps (one per 32 TMEM lanes) read each accumulator,
 //      free its stage, and accumulate P * (xs[m,kb] * ws[nt,kb]) in fp32
 //      registers (the per-K-block rescale of the page).
@@ -42,7 +48,7 @@
 //      fixed order, so results are deterministic -- and writes bf16 Y.
 // A call's epoch is one more than the workspace's epoch word for the CTA's
 // index; every CTA moves the words of its index class on to it when it ends,
-// so all words stay equal and every flag set by an earlier call is older.
+// so all words stay equal and every word or flag of an earlier call is older.
 // Every wait is bounded; on expiry the kernel records FP8BS_ERR_TIMEOUT in the
 // workspace error word, drains its own copies and MMAs (again bounded), frees
 // TMEM and returns.  The code of each role is kept small (rolled loops): the
@@ -143,13 +149,34 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t* kb_flags(const Params& p, uint32_t kb) {
-    return reinterpret_cast<uint32_t*>(p.act + kb * kKbRecBytes + kKbRecFlags);
+// Activation words of K block kb: scales [32 rows], codes [32 rows][32 words].
+__device__ __forceinline__ uint64_t* kb_scales(const Params& p, uint32_t kb) {
+    return reinterpret_cast<uint64_t*>(p.act + kb * kKbRecBytes + kKbRecScales);
 }
-__device__ __forceinline__ uint32_t* kb_scales(const Params& p, uint32_t kb) {
-    return reinterpret_cast<uint32_t*>(p.act + kb * kKbRecBytes + kKbRecScales);
+__device__ __forceinline__ uint64_t* kb_codes(const Params& p, uint32_t kb) {
+    return reinterpret_cast<uint64_t*>(p.act + kb * kKbRecBytes + kKbRecCodes);
 }
-__device__ __forceinline__ uint8_t* kb_codes(const Params& p, uint32_t kb) { return p.act + kb * kKbRecBytes + kKbRecCodes; }
+
+__device__ __forceinline__ uint64_t tag(uint32_t data, uint32_t epoch) {
+    return static_cast<uint64_t>(data) | (static_cast<uint64_t>(epoch) << 32);
+}
+__device__ __forceinline__ bool tagged(uint64_t w, uint32_t epoch) { return static_cast<uint32_t>(w >> 32) == epoch; }
+
+// Single-copy-atomic 64-bit exchange words (relaxed, GPU scope).
+__device__ __forceinline__ void st_pair(uint64_t* p, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ld_pair(const uint64_t* p, uint64_t& a, uint64_t& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_word(uint64_t* p, uint64_t a) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
+    uint64_t a;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+    return a;
+}
 
 // Cold path of every bounded wait.
 __device__ __noinline__ void raise_timeout(uint32_t* err, volatile uint32_t* misc) {
@@ -170,6 +197,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const P
         }
     }
     return true;
+}
+
+// Bookkeeping of a bounded poll begun at t0: true once the CTA has aborted,
+// or (recorded) once the wait has run past the limit.
+__device__ __forceinline__ bool gave_up(long long t0, const Params& p, volatile uint32_t* misc) {
+    if (misc[kMiscAbort] != 0) return true;
+    if (clock64() - t0 > p.timeout) {
+        raise_timeout(p.err, misc);
+        return true;
+    }
+    return false;
 }
 
 // Teardown drain: ignores the abort flag, still bounded.
@@ -314,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
 
     // ---- set-up; the first ring tiles go out at once ---------------------------
     if (tid == 0) {
-        // arrivals per unit: one per 16-byte code slice (local quant) or one per
-        // copied group (exchange)
-        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (SRC == kSrcLocal ? 16 : 1);
+        // arrivals per unit: one per 16-byte code slice (local quant), one per
+        // 8-code chunk and one per scale (exchange), or one per copied group
+        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (SRC == kSrcLocal ? 16 : (SRC == kSrcExchange ? 17 : 1));
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
@@ -472,58 +510,121 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                     if (valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
                 }
                 const SliceQuant qs = quant_slice<KIND>(raw, sTab);
-                if (valid) {
-                    *reinterpret_cast<uint2*>(kb_codes(p, kb) + m * 128 + l16 * 8) = make_uint2(qs.lo, qs.hi);
+                if (valid) {  // no fence, no flag: each word carries the epoch
+                    st_pair(kb_codes(p, kb) + m * 32 + 2 * l16, tag(qs.lo, epoch), tag(qs.hi, epoch));
                     if (l16 == 0)
-                        kb_scales(p, kb)[m] = KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale);
+                        st_word(kb_scales(p, kb) + m, tag(KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale),
+                                                          epoch));
                     put_xq_out<KIND>(p, m, kb, l16, qs);
-                    __threadfence();
                 }
-                __syncwarp();
-                if (valid && l16 == 0) ptx::st_release_u32(kb_flags(p, kb) + m, epoch);
             }
             // ---- 2b. the groups of this CTA's units into shared memory -------------
-            // group gi = i * M + m; thread qt takes gi = qt + 192 j: wait for its
-            // flags, put all its copies in flight, then one wait.
+            // chunk t = gi * 16 + l (group gi = i * M + m, 8 codes l): thread qt
+            // takes t = qt + 160 j, in rounds of kRound loads in flight; the stale
+            // ones are re-read together (one round trip per attempt, bounded)
+            // until both words carry the epoch.  Then the scales, the same way.
+            constexpr int kRound = 8;
             const int ngc = cnt * p.M;
+            const int nch = ngc * 16;
             bool ok = true;
+#pragma unroll 1
+            for (int base = 0; base < nch && ok; base += kQuantThreads * kRound) {
+                uint64_t w[kRound][2];
 #pragma unroll
-            for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                const int gi = qt + kQuantThreads * j;
-                if (ok && gi < ngc) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                    const int m = gi - i * p.M;
-                    ok = wait_flag(kb_flags(p, static_cast<uint32_t>(sKb[i])) + m, epoch, p, misc);
+                for (int j = 0; j < kRound; ++j) {
+                    const int t = base + qt + kQuantThreads * j;
+                    w[j][0] = w[j][1] = tag(0, epoch);  // out of range: nothing to wait for
+                    if (t < nch) {
+                        const int gi = t >> 4, l = t & 15;
+                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                        const int m = gi - i * p.M;
+                        ld_pair(kb_codes(p, static_cast<uint32_t>(sKb[i])) + m * 32 + 2 * l, w[j][0], w[j][1]);
+                    }
+                }
+                const long long t0 = clock64();
+                while (true) {
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < kRound; ++j) all = all && tagged(w[j][0], epoch) && tagged(w[j][1], epoch);
+                    if (all) break;
+                    if (gave_up(t0, p, misc)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < kRound; ++j) {
+                        const int t = base + qt + kQuantThreads * j;
+                        if (!(tagged(w[j][0], epoch) && tagged(w[j][1], epoch))) {
+                            const int gi = t >> 4, l = t & 15;
+                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                            const int m = gi - i * p.M;
+                            ld_pair(kb_codes(p, static_cast<uint32_t>(sKb[i])) + m * 32 + 2 * l, w[j][0], w[j][1]);
+                        }
+                    }
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int j = 0; j < kRound; ++j) {
+                    const int t = base + qt + kQuantThreads * j;
+                    if (t < nch) {
+                        const int gi = t >> 4, l = t & 15;
+                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                        const int m = gi - i * p.M;
+                        uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
+                        *reinterpret_cast<uint2*>(row + (((l >> 1) ^ (m & 7)) << 4) + ((l & 1) << 3)) =
+                            make_uint2(static_cast<uint32_t>(w[j][0]), static_cast<uint32_t>(w[j][1]));
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+#pragma unroll
+                for (int j = 0; j < kRound; ++j) {
+                    const int t = base + qt + kQuantThreads * j;
+                    if (t < nch) ptx::mbar_arrive(&bready[static_cast<int>(div_m(static_cast<uint32_t>(t >> 4), p.mdiv))]);
                 }
             }
             if (ok) {
-                uint32_t sbits[C::kGroupsPerThread];
+                uint64_t sw[C::kGroupsPerThread];
 #pragma unroll
                 for (int j = 0; j < C::kGroupsPerThread; ++j) {
                     const int gi = qt + kQuantThreads * j;
-                    sbits[j] = 0;
+                    sw[j] = tag(0, epoch);
                     if (gi < ngc) {
                         const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
                         const int m = gi - i * p.M;
-                        const uint32_t kb = static_cast<uint32_t>(sKb[i]);
-                        const uint8_t* src = kb_codes(p, kb) + m * 128;
-                        uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll 1
-                        for (int ch = 0; ch < 8; ++ch) ptx::cp_async16(row + ((ch ^ (m & 7)) << 4), src + ch * 16);
-                        sbits[j] = kb_scales(p, kb)[m];
+                        sw[j] = ld_word(kb_scales(p, static_cast<uint32_t>(sKb[i])) + m);
                     }
                 }
-                ptx::cp_async_wait_all();
+                const long long t0 = clock64();
+                while (true) {
+                    bool all = true;
 #pragma unroll
-                for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                    const int gi = qt + kQuantThreads * j;
-                    if (gi < ngc) {
-                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                        const int m = gi - i * p.M;
-                        sXs[i * MPAD + m] =
-                            KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(sbits[j]) : __uint_as_float(sbits[j]);
-                        ptx::fence_proxy_async_smem();
-                        ptx::mbar_arrive(&bready[i]);
+                    for (int j = 0; j < C::kGroupsPerThread; ++j) all = all && tagged(sw[j], epoch);
+                    if (all) break;
+                    if (gave_up(t0, p, misc)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                        const int gi = qt + kQuantThreads * j;
+                        if (!tagged(sw[j], epoch)) {
+                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                            const int m = gi - i * p.M;
+                            sw[j] = ld_word(kb_scales(p, static_cast<uint32_t>(sKb[i])) + m);
+                        }
+                    }
+                }
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < C::kGroupsPerThread; ++j) {
+                        const int gi = qt + kQuantThreads * j;
+                        if (gi < ngc) {
+                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
+                            const int m = gi - i * p.M;
+                            const uint32_t bits = static_cast<uint32_t>(sw[j]);
+                            sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(bits) : __uint_as_float(bits);
+                            ptx::mbar_arrive(&bready[i]);
+                        }
                     }
                 }
             }
