@@ -118,7 +118,7 @@ struct Params {
     uint32_t* err;
     uint32_t* gen;            // epoch words
     uint32_t* pflag;          // partial flags [CTA][4 epilogue warps]
-    float* slots;             // partial slots [CTA][32 columns][128 rows]
+    uint64_t* slots;          // partial slots [CTA][32 columns][128 rows]: tagged words or fp32
     uint8_t* act;             // activation records [K/128][kKbRecBytes]
     uint8_t* xq_out;
     void* xs_out;
@@ -238,16 +238,38 @@ __device__ __forceinline__ void store_y(const Params& p, int n, const float (&v)
         if (m < p.M) p.y[m * p.ldy + n] = f32_to_bf16_rn(v[m]);
 }
 
+// Calls of up to this many tokens exchange split-K partials as tagged words;
+// larger ones as fp32 with a flag per epilogue warp.  A tagged reader needs
+// one round of loads per kTaggedRound words, a flagged one a single wait and
+// one copy, plus the writer's fence.
+constexpr int kTaggedMaxM = 8;
+constexpr int kTaggedRound = 16;
+
+// Word of the partial (contributor b + t / M, column t % M, row r).
+__device__ __forceinline__ const uint64_t* partial_word(const Params& p, uint32_t b, int t, int r) {
+    const int j = static_cast<int>(div_m(static_cast<uint32_t>(t), p.mdiv));
+    const int m = t - j * p.M;
+    return p.slots + static_cast<size_t>(b + j) * (32 * 128) + m * 128 + r;
+}
+
+__device__ __forceinline__ float* fp32_slot(const Params& p, uint32_t b) {
+    return reinterpret_cast<float*>(p.slots + static_cast<size_t>(b) * (32 * 128));
+}
+
 // Output of one n-tile's accumulator by one epilogue warp (rows q*32 .. +31).
 // role 0: this CTA owns the tile's whole K range -> bf16 Y.
 // role 1: a later contributor -> write the partial of these rows into this
-//         CTA's slot, then set this warp's flag.
-// role 2: the reducer -> copy the later contributors' partials of these rows
-//         (in batches that fit this warp's quarter of the idle weight ring),
-//         sum in CTA order, bf16 Y.
-// Returns false if a wait gave up.
-template <int MPAD, int STAGE_FLOATS>
-__device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (&acc)[MPAD], uint32_t c, uint32_t G,
+//         CTA's slot: tagged words (no fence, no flag) or fp32 and then this
+//         warp's flag.
+// role 2: the reducer -> gather the later contributors' partials of these
+//         rows (batches that fit this warp's quarter of the idle weight ring),
+//         sum in CTA order, bf16 Y.  Tagged words are read in rounds of loads
+//         in flight, the stale ones re-read together until they carry the
+//         epoch; fp32 partials are copied (cp.async) once their flags carry it.
+// last: the CTA that holds the tile's last unit.  Returns false if a wait
+// gave up.
+template <int MPAD, int STAGE_FLOATS, bool TAGGED>
+__device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (&acc)[MPAD], uint32_t c, uint32_t last,
                                         int role, int q, int lane, uint32_t epoch, volatile uint32_t* misc,
                                         float* stage) {
     const int r = q * 32 + lane;
@@ -257,16 +279,22 @@ __device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (
         return true;
     }
     if (role == 1) {
-        float* slot = p.slots + static_cast<size_t>(c) * (32 * 128);
+        if constexpr (TAGGED) {
+            uint64_t* slot = p.slots + static_cast<size_t>(c) * (32 * 128);
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m)
-            if (m < p.M) slot[m * 128 + r] = acc[m];
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) ptx::st_release_u32(p.pflag + c * 4 + q, epoch);
+            for (int m = 0; m < MPAD; ++m)
+                if (m < p.M) st_word(slot + m * 128 + r, tag(__float_as_uint(acc[m]), epoch));
+        } else {
+            float* slot = fp32_slot(p, c);
+#pragma unroll
+            for (int m = 0; m < MPAD; ++m)
+                if (m < p.M) slot[m * 128 + r] = acc[m];
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) ptx::st_release_u32(p.pflag + c * 4 + q, epoch);
+        }
         return true;
     }
-    const uint32_t last = cta_of((nt + 1) * static_cast<uint32_t>(p.KB) - 1, p.T, G);
     const int per = p.M * 32;               // floats per contributor (this warp's rows)
     const int batch = STAGE_FLOATS / per;   // contributors per batch (>= 4)
     float* st = stage + q * STAGE_FLOATS;   // this warp's quarter of the ring
@@ -274,18 +302,46 @@ __device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (
     for (uint32_t b = c + 1; b <= last; b += batch) {
         const int nb = static_cast<int>(last + 1 - b) < batch ? static_cast<int>(last + 1 - b) : batch;
         bool ok = true;
-        if (lane < nb) ok = wait_flag(p.pflag + (b + lane) * 4 + q, epoch, p, misc);
-        if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-        // 16-byte chunks: (contributor j, column m, rows 4k .. 4k+3 of this warp)
+        if constexpr (TAGGED) {
+            const int nw = nb * p.M;        // this lane's words: t = j * M + m
 #pragma unroll 1
-        for (int t = lane; t < nb * p.M * 8; t += 32) {
-            const int jm = t >> 3, k = t & 7;
-            const int j = jm / p.M;
-            const int m = jm - j * p.M;
-            ptx::cp_async16(st + jm * 32 + 4 * k,
-                            p.slots + static_cast<size_t>(b + j) * (32 * 128) + m * 128 + q * 32 + 4 * k);
+            for (int base = 0; base < nw && ok; base += kTaggedRound) {
+                uint64_t w[kTaggedRound];
+#pragma unroll
+                for (int k = 0; k < kTaggedRound; ++k)
+                    w[k] = base + k < nw ? ld_word(partial_word(p, b, base + k, r)) : tag(0, epoch);
+                const long long t0 = clock64();
+                while (true) {
+                    bool all = true;
+#pragma unroll
+                    for (int k = 0; k < kTaggedRound; ++k) all = all && tagged(w[k], epoch);
+                    if (all) break;
+                    if (gave_up(t0, p, misc)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kTaggedRound; ++k)
+                        if (!tagged(w[k], epoch)) w[k] = ld_word(partial_word(p, b, base + k, r));
+                }
+#pragma unroll
+                for (int k = 0; k < kTaggedRound; ++k)
+                    if (base + k < nw) st[(base + k) * 32 + lane] = __uint_as_float(static_cast<uint32_t>(w[k]));
+            }
+            if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+        } else {
+            if (lane < nb) ok = wait_flag(p.pflag + (b + lane) * 4 + q, epoch, p, misc);
+            if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+            // 16-byte chunks: (contributor j, column m, rows 4k .. 4k+3 of this warp)
+#pragma unroll 1
+            for (int t = lane; t < nb * p.M * 8; t += 32) {
+                const int jm = t >> 3, k = t & 7;
+                const int j = jm / p.M;
+                const int m = jm - j * p.M;
+                ptx::cp_async16(st + jm * 32 + 4 * k, fp32_slot(p, b + j) + m * 128 + q * 32 + 4 * k);
+            }
+            ptx::cp_async_wait_all();
         }
-        ptx::cp_async_wait_all();
         __syncwarp();
 #pragma unroll 1
         for (int j = 0; j < nb; ++j) {
@@ -324,7 +380,7 @@ __device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t
     }
 }
 
-template <int MPAD, int KIND, int SRC>
+template <int MPAD, int KIND, int SRC, bool TAGGED>
 __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MPAD, SRC>;
     constexpr int S = C::kStages;
@@ -675,6 +731,11 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
 #pragma unroll
             for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
             uint32_t cur = nt0, kb = kb0;
+            // the CTAs holding the last units of this CTA's first and last tiles
+            // (only those two can be shared with other CTAs)
+            const uint32_t ntl = nt0 + (kb0 + static_cast<uint32_t>(cnt) - 1) / static_cast<uint32_t>(KB);
+            const uint32_t last0 = cta_of((nt0 + 1) * static_cast<uint32_t>(KB) - 1, p.T, G);
+            const uint32_t lastl = cta_of((ntl + 1) * static_cast<uint32_t>(KB) - 1, p.T, G);
 #pragma unroll 1
             for (int i = 0; i < cnt; ++i) {
                 const int a = i % kAccStages;
@@ -710,8 +771,9 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                     const bool starts_here = cur != nt0 || kb0 == 0;
                     const bool ends_here = kb == KB;
                     const int role = starts_here ? (ends_here ? 0 : 2) : 1;
-                    if (hdr_ok && !flush_tile<MPAD, C::kRingBytes / 16>(p, cur, acc, c, G, role, q, lane, epoch,
-                                                                         misc, reinterpret_cast<float*>(sRing)))
+                    if (hdr_ok && !flush_tile<MPAD, C::kRingBytes / 16, TAGGED>(p, cur, acc, c, cur == nt0 ? last0 : lastl,
+                                                                                 role, q, lane, epoch, misc,
+                                                                                 reinterpret_cast<float*>(sRing)))
                         break;
 #pragma unroll
                     for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
@@ -751,10 +813,10 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
         for (uint32_t j = c + lane * G; j < static_cast<uint32_t>(kMaxCtas); j += 32 * G) p.gen[j] = epoch;
 }
 
-template <int MPAD, int KIND, int SRC>
+template <int MPAD, int KIND, int SRC, bool TAGGED>
 cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     using C = Cfg<MPAD, SRC>;
-    auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC>;
+    auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC, TAGGED>;
     // Opt in to the dynamic shared memory once per device (not a stream
     // operation, so it is harmless during graph capture too).
     static int configured[64] = {0};
@@ -779,7 +841,7 @@ cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int MPAD, int KIND, int SRC>
+template <int MPAD, int KIND, int SRC, bool TAGGED>
 cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
     // At most one CTA per SM with at most kUnits units each: weights with more
     // units than that go in several launches of whole n-tiles.
@@ -797,7 +859,7 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
         p.xs_out = nt_base == 0 ? a.xs_out : nullptr;
         p.pdl = nt_base == 0 ? a.pdl : 1;  // later chunks follow our own launch, which never writes packed
         const int grid = static_cast<int>(p.T) < a.sm_count ? static_cast<int>(p.T) : a.sm_count;
-        const cudaError_t e = launch_impl<MPAD, KIND, SRC>(p, grid, stream);
+        const cudaError_t e = launch_impl<MPAD, KIND, SRC, TAGGED>(p, grid, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -806,12 +868,14 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
 template <int KIND>
 cudaError_t launch_kind(const Params& p, const FusedArgs& a, cudaStream_t stream) {
     if (a.xq_in) {
-        if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput>(p, a, stream);
-        return launch_chunks<32, KIND, kSrcInput>(p, a, stream);
+        if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcInput, true>(p, a, stream);
+        if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput, false>(p, a, stream);
+        return launch_chunks<32, KIND, kSrcInput, false>(p, a, stream);
     }
-    if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, kSrcLocal>(p, a, stream);
-    if (a.M <= 16) return launch_chunks<16, KIND, kSrcExchange>(p, a, stream);
-    return launch_chunks<32, KIND, kSrcExchange>(p, a, stream);
+    if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, kSrcLocal, true>(p, a, stream);
+    if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcExchange, true>(p, a, stream);
+    if (a.M <= 16) return launch_chunks<16, KIND, kSrcExchange, false>(p, a, stream);
+    return launch_chunks<32, KIND, kSrcExchange, false>(p, a, stream);
 }
 
 }  // namespace
@@ -831,7 +895,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.err = reinterpret_cast<uint32_t*>(a.workspace);
     p.gen = reinterpret_cast<uint32_t*>(a.workspace + ws_gen_offset());
     p.pflag = reinterpret_cast<uint32_t*>(a.workspace + ws_pflag_offset());
-    p.slots = reinterpret_cast<float*>(a.workspace + ws_partials_offset());
+    p.slots = reinterpret_cast<uint64_t*>(a.workspace + ws_partials_offset());
     p.act = a.workspace + ws_act_offset(a.sm_count);
     p.xq_in = a.xq_in;
     p.ldxq = a.ldxq;

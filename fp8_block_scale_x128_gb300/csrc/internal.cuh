@@ -35,25 +35,27 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
 
 // Workspace layout (bytes).  The CTAs of one fused launch exchange two kinds
 // of data through it: the quantised activations (each 1x128 group published
-// once, by one CTA) and the split-K partials.  The activations travel as
-// 64-bit words, 32 data bits and the call's 32-bit epoch, so a reader sees
-// either an older word or the new one and needs no flag; each split-K slot
-// has a flag per epilogue warp that its writer sets to the epoch after the
-// data.  Words and flags left by earlier calls carry older epochs, so nothing
-// is cleared between calls.  Every region sits at a place that depends on sm_count only,
-// never on N or K, so a workspace serves calls of any shape without a flag of
-// one call ever landing on the data of another.
+// once, by one CTA) and the split-K partials.  The activations, and the
+// partials of a tile with few of them, travel as 64-bit words, 32 data bits
+// and the call's 32-bit epoch, so a reader sees either an older word or the
+// new one and needs no flag.  The partials of other tiles are plain fp32,
+// followed by a flag per epilogue warp set to the epoch.  Words and flags
+// left by earlier calls carry older epochs, so nothing is cleared between
+// calls.  Every region sits at a place that depends on sm_count only, never
+// on N or K, so a workspace serves calls of any shape without a word of one
+// call ever being taken for one of another.
 //   [0, 256)                  device error word
 //   [256, +4 KB)              epoch words, one per possible CTA index
 //   [4352, +16 KB)            partial flags, one per (CTA index, epilogue warp)
-//   then sm_count x 16 KB     split-K partial slots, fp32 [32 columns][128 rows]
+//   then sm_count x 32 KB     split-K partial slots, [32 columns][128 rows] of
+//                             tagged words or (first 16 KB) of fp32
 //   then K/128 x 8448 B       one record per K block of the activations:
 //                             32 scale words, 32 rows x 32 words of 4 codes
 constexpr size_t kWsErrorBytes = 256;
 constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
 constexpr size_t kWsGenBytes = kMaxCtas * sizeof(uint32_t);
 constexpr size_t kWsPflagBytes = kMaxCtas * 4 * sizeof(uint32_t);
-constexpr size_t kSlotBytes = 32 * 128 * sizeof(float);
+constexpr size_t kSlotBytes = 32 * 128 * sizeof(uint64_t);
 constexpr size_t kKbRecScales = 0;                       // within a K-block record
 constexpr size_t kKbRecCodes = 32 * sizeof(uint64_t);
 constexpr size_t kKbRecBytes = kKbRecCodes + 32 * 32 * sizeof(uint64_t);

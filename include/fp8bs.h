@@ -164,8 +164,8 @@ enum {
 /* Workspace bytes the fused GEMM needs for an N x K weight on a device with
  * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
  * CUDA device): a 256-byte error word, 4 KB of epoch words, 16 KB of
- * split-K flags, one 16 KB split-K slot per multiprocessor and 8.25 KB per 128
- * columns of K for the quantised activations the CTAs exchange.  The size
+ * split-K flags, one 32 KB split-K slot per multiprocessor and 8.25 KB per
+ * 128 columns of K for the quantised activations the CTAs exchange.  The size
  * depends on K and sm_count only and every region sits at a place that
  * depends on sm_count only, so a workspace sized for the largest K serves
  * every weight of that K or less.  Returns 0 for an
@@ -236,7 +236,7 @@ int fp8bs_check_error(void* workspace, void* stream);
 #define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */
 
 /* fp8bs_gemm_fused without a workspace argument: the scratch lives in one
- * fixed device array inside this library (3,723,520 bytes per device,
+ * fixed device array inside this library (6,344,960 bytes per device,
  * sized for FP8BS_STATIC_MAX_SMS CTAs and K up to FP8BS_STATIC_MAX_K), so the
  * call allocates no device memory, ever.  It is meant for callers that cannot
  * allocate or own device memory: an operator plugged into a runtime whose

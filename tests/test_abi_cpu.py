@@ -52,7 +52,7 @@ def test_packed_weight_bytes(L):
 
 def test_workspace_bytes_for_explicit_sm_count(L):
     def expect(K, sm):
-        return 256 + 4096 + 16384 + sm * 32 * 128 * 4 + (K // 128) * (32 * 8 + 32 * 32 * 8)
+        return 256 + 4096 + 16384 + sm * 32 * 128 * 8 + (K // 128) * (32 * 8 + 32 * 32 * 8)
     assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == expect(4096, 152)
     assert fb.fp8bs_workspace_bytes(128, 128, 152) == expect(128, 152)
     # independent of N
