@@ -43,9 +43,11 @@
 //      registers (the per-K-block rescale of the page).
 //   5. An n-tile whose whole K range the CTA owns is written as bf16 Y.
 //      Otherwise the tile's first CTA reduces it: each later contributor
-//      writes its fp32 partial into its slot and sets the slot's flags; the
-//      reducer copies the partials (cp.async) and sums them in CTA order -- a
-//      fixed order, so results are deterministic -- and writes bf16 Y.
+//      writes its partial into its slot, either as tagged words (up to 8
+//      tokens; no fence, no flag) or as fp32 followed by the slot's flags; the
+//      reducer gathers the partials (polled words, or cp.async once the flags
+//      are set) and sums them in CTA order -- a fixed order, so results are
+//      deterministic -- and writes bf16 Y.
 // A call's epoch is one more than the workspace's epoch word for the CTA's
 // index; every CTA moves the words of its index class on to it when it ends,
 // so all words stay equal and every word or flag of an earlier call is older.
