@@ -43,7 +43,7 @@
 //      registers (the per-K-block rescale of the page).
 //   5. An n-tile whose whole K range the CTA owns is written as bf16 Y.
 //      Otherwise the tile's first CTA reduces it: each later contributor
-//      writes its partial into its slot, either as tagged words (up to 8
+//      writes its partial into its slot, either as tagged words (up to 12
 //      tokens; no fence, no flag) or as fp32 followed by the slot's flags; the
 //      reducer gathers the partials (polled words, or cp.async once the flags
 //      are set) and sums them in CTA order -- a fixed order, so results are
@@ -244,7 +244,7 @@ __device__ __forceinline__ void store_y(const Params& p, int n, const float (&v)
 // larger ones as fp32 with a flag per epilogue warp.  A tagged reader needs
 // one round of loads per kTaggedRound words, a flagged one a single wait and
 // one copy, plus the writer's fence.
-constexpr int kTaggedMaxM = 8;
+constexpr int kTaggedMaxM = 12;
 constexpr int kTaggedRound = 16;
 
 // Word of the partial (contributor b + t / M, column t % M, row r).

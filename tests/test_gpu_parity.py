@@ -212,14 +212,14 @@ def test_fused_small_shapes(dev, oracle_mod, kind, M, N, K):
     run_fused(oracle_mod, dev, M, N, K, kind, seed=M * 131 + N + K)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8, 9])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8, 12, 13])
 @pytest.mark.parametrize("N,K,kind", [(128, 128, F32), (384, 640, F32), (640, 2048, UE8), (5120, 4096, F32),
                                       (4608, 4096, F32), (4096, 2048, F32), (7168, 2048, UE8),
                                       (1536, 7168, UE8), (4096, 4096, UE8)])
 def test_fused_few_tokens(dev, oracle_mod, N, K, kind, M):
     # the local-quant variant (up to 6 tokens), the exchange variant with tagged
-    # split-K partials (7, 8) and with flagged ones (9) on every benchmark shape
-    # and a few small ones, quant bytes included
+    # split-K partials (7 to 12) and with flagged ones (13) on every benchmark
+    # shape and a few small ones, quant bytes included
     run_fused(oracle_mod, dev, M, N, K, kind, seed=5000 + 7 * M + N // 128 + K // 128)
 
 
@@ -274,7 +274,7 @@ def test_prequant_gemm_against_oracle(dev, oracle_mod, kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", [F32, UE8])
-@pytest.mark.parametrize("M", [1, 6, 7, 8, 9, 16, 17, 32])
+@pytest.mark.parametrize("M", [1, 6, 7, 12, 13, 16, 17, 32])
 def test_two_launch_path_is_bit_identical_to_fused(dev, kind, M):
     # fp8bs_quant + fp8bs_gemm_prequant runs the same MMAs, rescale and split-K
     # order as the fused call on the same x
