@@ -13,7 +13,8 @@ from these pages:
   the 128x128 block scale applied to each partial sum.
 * "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense 128x128 fp8
   linears (6/8)", "Motivation" / "Modifications" -- power-of-two (e8m0)
-  weight scales and ue8m0 activation scales.
+  weight scales and ue8m0 activation scales, emitted by the fused
+  input_norm / q_norm (RMSNorm) producers.
 
 It shares no code with the CUDA library and never imports it.
 """
@@ -85,6 +86,11 @@ def _load():
         lib.oracle_linear.argtypes = [vp, i64, i64, i64, vp, vp, i64, c.c_int, vp, vp, vp,
                                       c.c_int]
         lib.oracle_linear.restype = c.c_int
+        lib.oracle_rmsnorm.argtypes = [vp, i64, i64, i64, vp, c.c_double, vp, vp]
+        lib.oracle_rmsnorm.restype = c.c_int
+        lib.oracle_rmsnorm_quant.argtypes = [vp, i64, i64, i64, vp, c.c_double, c.c_int, vp, vp,
+                                             vp]
+        lib.oracle_rmsnorm_quant.restype = c.c_int
         _lib = lib
         return lib
 
@@ -209,6 +215,39 @@ def linear(x_bf16, wq, ws, kind: int = SCALE_F32, nthreads: int = 1):
                                _ptr(xs), _ptr(y), int(nthreads))
     if rc:
         raise ValueError("oracle_linear rejected its arguments")
+    return y, xq, xs
+
+
+def rmsnorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float):
+    """RMSNorm of each row (x * gamma / sqrt(mean x^2 + eps)) in fp64.
+
+    Returns (y fp64 [M, K], y rounded to bf16 bits uint16 [M, K])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16)
+    M, K = x.shape
+    assert g.shape == (K,)
+    y64 = np.empty((M, K), dtype=np.float64)
+    y = np.empty((M, K), dtype=np.uint16)
+    rc = _load().oracle_rmsnorm(_ptr(x), M, K, K, _ptr(g), float(eps), _ptr(y64), _ptr(y))
+    if rc:
+        raise ValueError("oracle_rmsnorm rejected its arguments")
+    return y64, y
+
+
+def rmsnorm_quant(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float, kind: int = SCALE_F32):
+    """The producer: RMSNorm rounded to bf16, then the 1x128 quant.
+
+    Returns (y bf16 bits [M, K], xq uint8 [M, K], xs [M, K/128])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16)
+    M, K = x.shape
+    y = np.empty((M, K), dtype=np.uint16)
+    xq = np.empty((M, K), dtype=np.uint8)
+    xs = np.empty((M, K // 128), dtype=_scale_dtype(kind))
+    rc = _load().oracle_rmsnorm_quant(_ptr(x), M, K, K, _ptr(g), float(eps), int(kind), _ptr(y),
+                                      _ptr(xq), _ptr(xs))
+    if rc:
+        raise ValueError("oracle_rmsnorm_quant rejected its arguments")
     return y, xq, xs
 
 

@@ -22,7 +22,8 @@
  *   [P4] "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense 128x128 fp8
  *        linears (6/8)", sections "Motivation" and "Modifications": power-of-two
  *        128x128 weight scales stored as one e8m0 byte per block, and ue8m0
- *        per-1x128 activation scales.
+ *        per-1x128 activation scales emitted by the fused input_norm / q_norm
+ *        (RMSNorm) producers.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - e4m3fn is the OCP FP8 E4M3 format: bias 7, no infinities, NaN = S.1111.111,
@@ -35,6 +36,8 @@
  *   - ue8m0 scale = the smallest power of two >= fp32(amax / 448), exponent
  *     clamped to [-127, 127], stored as the byte exponent + 127.
  *   - the fp64 result is rounded straight to bf16, nearest-even.
+ *   - the RMSNorm producer normalises each whole row, x * gamma /
+ *     sqrt(mean x^2 + eps), rounds that to bf16 and quantises the bf16 values.
  *
  * Build: gcc -O2 -fPIC -shared -ffp-contract=off -pthread (no fast-math: every
  * fp32 operation below must be the IEEE one).
@@ -367,3 +370,51 @@ int oracle_linear(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const ui
 
 /* Bit helpers exposed for tests of the rounding rules. */
 uint32_t oracle_f32_bits(float f) { return f32_to_bits(f); }
+
+/* ------------------------------------------------------------------------- */
+/* RMSNorm producer [P4 "Modifications": the fused input_norm / q_norm       */
+/* producers emit the ue8m0 (or fp32) 1x128 scales of the normalised         */
+/* activations, so the quant adds no launch]                                 */
+/* ------------------------------------------------------------------------- */
+
+/* Readings (the pages name the producer but print no formula):
+ *   - RMSNorm over the whole row of K values:
+ *       y[m,k] = x[m,k] * gamma[k] / sqrt(mean_k x[m,k]^2 + eps),
+ *     x and gamma bf16, evaluated here in fp64;
+ *   - the producer's output activation is that value rounded to bf16
+ *     (nearest-even), and the 1x128 quant above takes those bf16 values, so the
+ *     fused producer gives the bytes of "RMSNorm, then quant".
+ * x: bf16 [M, K], row stride ldx.  gamma: bf16 [K].  y64: fp64 [M, K] (nullable),
+ * y: bf16 [M, K] (nullable), both row stride K.  Returns 0, or -1 on a bad shape
+ * or a negative eps. */
+int oracle_rmsnorm(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint16_t* gamma,
+                   double eps, double* y64, uint16_t* y) {
+    if (M < 0 || K <= 0 || ldx < K || !(eps >= 0.0)) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)oracle_bf16_to_f32(x[m * ldx + k]);
+            ss += v * v;
+        }
+        double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)oracle_bf16_to_f32(x[m * ldx + k]);
+            double g = (double)oracle_bf16_to_f32(gamma[k]);
+            double r = rms > 0.0 ? v * g / rms : 0.0 * v * g; /* zero row, eps 0: signed zero */
+            if (y64) y64[m * K + k] = r;
+            if (y) y[m * K + k] = oracle_f64_to_bf16(r);
+        }
+    }
+    return 0;
+}
+
+/* The producer: RMSNorm (above), rounded to bf16, then the 1x128 quant.
+ * y: bf16 [M, K] scratch/output the caller provides; xq [M, K]; xs [M, K/128]. */
+int oracle_rmsnorm_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                         const uint16_t* gamma, double eps, int kind, uint16_t* y, uint8_t* xq,
+                         void* xs) {
+    if (K % 128 != 0) return -1;
+    int rc = oracle_rmsnorm(x, M, K, ldx, gamma, eps, NULL, y);
+    if (rc) return rc;
+    return oracle_quant_1x128(y, M, K, K, kind, xq, xs);
+}

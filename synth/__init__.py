@@ -13,6 +13,8 @@ Recipes:
         chosen with probability 1% and multiplied by 20 (outliers), then
         rounded to bf16 (nearest even).
   W  -- fp32 [N, K]: N(0, 0.02).
+  gamma -- bf16 [K], the RMSNorm weight of the producer: fp32 1 + 0.25 * N(0, 1),
+        rounded to bf16 (nearest even).
 Seeds: ``seed = 1000 * workload + copy`` by convention of the callers.
 """
 
@@ -51,6 +53,16 @@ def w_f32(N: int, K: int, seed: int) -> np.ndarray:
     rng = _rng(seed)
     return (rng.standard_normal((N, K), dtype=np.float32) * np.float32(WEIGHT_STD)).astype(
         np.float32)
+
+
+GAMMA_STD = 0.25
+
+
+def gamma_bf16(K: int, seed: int) -> np.ndarray:
+    """RMSNorm weight as bf16 bit patterns, uint16 [K] ~ 1 + N(0, 0.25)."""
+    rng = _rng(seed)
+    v = (np.float32(1.0) + rng.standard_normal(K, dtype=np.float32) * np.float32(GAMMA_STD))
+    return f32_to_bf16_bits(v.astype(np.float32))
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:

@@ -419,3 +419,99 @@ def test_linear_is_quant_then_gemm(oracle_mod):
         xq2, xs2 = oracle_mod.quant_1x128(x, kind)
         assert np.array_equal(xq, xq2) and np.array_equal(xs, xs2)
         assert np.array_equal(y, oracle_mod.gemm(xq2, xs2, wq, ws, kind))
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm producer ("[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense
+# 128x128 fp8 linears (6/8)", "Modifications": the fused input_norm / q_norm
+# producers emit the 1x128 scales).  Reading: y = x * gamma / sqrt(mean x^2 +
+# eps), rounded to bf16, then the 1x128 quant of those bf16 values.
+# ---------------------------------------------------------------------------
+
+BF16_ONE = 0x3F80
+
+
+def bf16_bits(vals):
+    return synth.f32_to_bf16_bits(np.asarray(vals, dtype=np.float32))
+
+
+def test_rmsnorm_three_four_five(oracle_mod):
+    # mean of squares (9 + 16) / 128, so y = x * sqrt(128) / 5 in closed form
+    x = np.zeros((1, 128), np.uint16)
+    x[0, :2] = bf16_bits([3.0, 4.0])
+    y64, _ = oracle_mod.rmsnorm(x, np.full(128, BF16_ONE, np.uint16), 0.0)
+    assert y64[0, 0] == pytest.approx(3.0 * math.sqrt(128.0) / 5.0, rel=1e-15)
+    assert y64[0, 1] == pytest.approx(4.0 * math.sqrt(128.0) / 5.0, rel=1e-15)
+    assert np.all(y64[0, 2:] == 0.0)
+
+
+@pytest.mark.parametrize("c", [0.375, -3.0, 1000.0])
+def test_rmsnorm_constant_row_is_its_sign(oracle_mod, c):
+    # every |x| equal -> rms = |x| -> y = sign(x) exactly (eps 0)
+    K = 256
+    x = np.tile(bf16_bits([c, -c]), (2, K // 2))
+    y64, y = oracle_mod.rmsnorm(x, np.full(K, BF16_ONE, np.uint16), 0.0)
+    assert np.all(y64[:, 0::2] == math.copysign(1.0, c)) and np.all(y64[:, 1::2] == -math.copysign(1.0, c))
+    assert np.all(y[:, 0::2] == (0x3F80 if c > 0 else 0xBF80))
+
+
+def test_rmsnorm_eps_enters_under_the_root(oracle_mod):
+    # mean x^2 = 1 and eps = 3 -> rms = 2 -> y = x / 2
+    K = 128
+    x = np.tile(bf16_bits([1.0, -1.0]), (1, K // 2))
+    y64, _ = oracle_mod.rmsnorm(x, np.full(K, BF16_ONE, np.uint16), 3.0)
+    assert np.all(y64[0, 0::2] == 0.5) and np.all(y64[0, 1::2] == -0.5)
+
+
+def test_rmsnorm_zero_row_is_zero(oracle_mod):
+    K = 256
+    x = np.zeros((1, K), np.uint16)
+    x[0, 1::2] = 0x8000  # -0.0
+    y64, y = oracle_mod.rmsnorm(x, synth.gamma_bf16(K, seed=3), 1e-6)
+    assert np.all(y64 == 0.0) and not np.any(np.isnan(y64))
+    _, xq, xs = oracle_mod.rmsnorm_quant(x, synth.gamma_bf16(K, seed=3), 1e-6)
+    assert np.all(xs == 0.0) and np.all(xq[0, 0::2] == 0x00) and np.all(xq[0, 1::2] == 0x80)
+
+
+def test_rmsnorm_power_of_two_scale_invariance(oracle_mod):
+    # eps 0: scaling a row by 2^j scales every x and the rms by 2^j exactly
+    K = 512
+    x = synth.x_bf16(3, K, seed=11)
+    g = synth.gamma_bf16(K, seed=12)
+    xs = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x) * np.float32(8.0))
+    a, ya = oracle_mod.rmsnorm(x, g, 0.0)
+    b, yb = oracle_mod.rmsnorm(xs, g, 0.0)
+    assert np.array_equal(a, b) and np.array_equal(ya, yb)
+
+
+def test_rmsnorm_gamma_multiplies_each_column(oracle_mod):
+    # y(gamma) = gamma * y(1) column by column, against a numpy restatement of
+    # the normalisation with unit weight
+    K = 384
+    x = synth.x_bf16(4, K, seed=21)
+    g = synth.gamma_bf16(K, seed=22)
+    y1, _ = oracle_mod.rmsnorm(x, np.full(K, BF16_ONE, np.uint16), 1e-6)
+    yg, _ = oracle_mod.rmsnorm(x, g, 1e-6)
+    gf = synth.bf16_bits_to_f32(g).astype(np.float64)
+    np.testing.assert_allclose(yg, y1 * gf[None, :], rtol=1e-14, atol=0)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    ref = xf / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(y1, ref, rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_quant_is_quant_of_the_rounded_norm(oracle_mod):
+    # the producer's bytes are those of the two steps in sequence, and the bf16
+    # output is the fp64 value rounded to nearest even by torch's cast
+    K = 640
+    x = synth.x_bf16(5, K, seed=31)
+    g = synth.gamma_bf16(K, seed=32)
+    for kind in (0, 1):
+        y, xq, xsc = oracle_mod.rmsnorm_quant(x, g, 1e-6, kind)
+        y64, yb = oracle_mod.rmsnorm(x, g, 1e-6)
+        assert np.array_equal(y, yb)
+        t = torch.from_numpy(y64).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(y, t)
+        q2, s2 = oracle_mod.quant_1x128(y, kind)
+        assert np.array_equal(xq, q2) and np.array_equal(xsc, s2)
+        if kind == 0:  # every non-zero group holds a byte of magnitude 0x7E
+            assert np.all((xq.reshape(5, K // 128, 128) & 0x7F).max(axis=2) == 0x7E)
