@@ -433,6 +433,83 @@ def per_m_table(fb, torch, dev, stream, pdl, two_launch=False):
     return out
 
 
+PRODUCER_DECODE = [(1, 7168), (4, 7168), (16, 7168), (32, 7168), (32, 4096), (32, 2048)]
+PRODUCER_LARGE = (16384, 7168)
+
+
+def producer_bytes(M: int, K: int, kind: int) -> int:
+    """Algorithmic bytes of one RMSNorm + quant call: x and gamma read, codes
+    and scales written (the optional bf16 y is not requested when timed)."""
+    return 2 * M * K + 2 * K + M * K + (M * K // 128) * (1 if kind == 1 else 4)
+
+
+def graph_us_per_call(torch, stream, fn, n_calls: int, reps: int, warm: int = 5) -> float:
+    """Capture n_calls of fn(i) in one CUDA graph; µs per call over reps replays."""
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            fn(i)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) * 1e3 / (reps * n_calls)
+
+
+def producer_table(fb, torch, dev, stream, peak: float):
+    """The fused RMSNorm + 1x128 quant producer (ue8m0 scales, as the page's
+    producer emits).  First, for the roofline, launches of 16384 x 7168 rows
+    over 2 rotated inputs (470 MB of x, larger than L2): 4 per graph, 5 warm-up
+    and 20 timed replays.  Then µs/call at decode sizes (rows L2-resident, 24
+    rotated inputs per graph, 50 replays)."""
+    import synth
+    kind = fb.FP8BS_SCALE_UE8M0
+    out = {"kind": "ue8m0", "eps": 1e-6}
+    M, K = PRODUCER_LARGE
+    g = synth.x_bf16_torch(1, K, seed=901, device=dev)[0].abs() + 0.5
+    xs_in = [synth.x_bf16_torch(M, K, seed=920 + c, device=dev) for c in range(2)]
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    xsc = torch.empty((M, K // 128), dtype=torch.uint8, device=dev)
+    us = graph_us_per_call(torch, stream, lambda i: fb.fp8bs_rmsnorm_quant(
+        xs_in[i % 2], g, 1e-6, kind, xq=xq, xs=xsc), 4, 20)
+    nbytes = producer_bytes(M, K, 1)
+    gbps = nbytes / us / 1e3
+    out["large"] = {"M": M, "K": K, "us": round(us, 2), "bytes": nbytes, "GBps": round(gbps, 1),
+                    "peak": peak, "frac": round(gbps / peak, 3),
+                    "kernel": "rmsnorm_quant_kernel", "bound": "hbm"}
+    del xs_in, xq, xsc
+    torch.cuda.empty_cache()
+    out["decode_us"] = {}
+    for (M, K) in PRODUCER_DECODE:
+        g = synth.x_bf16_torch(1, K, seed=900, device=dev)[0].abs() + 0.5
+        xs_in = [synth.x_bf16_torch(M, K, seed=910 + c, device=dev) for c in range(COPIES)]
+        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        xsc = torch.empty((M, K // 128), dtype=torch.uint8, device=dev)
+        us = graph_us_per_call(torch, stream, lambda i: fb.fp8bs_rmsnorm_quant(
+            xs_in[i], g, 1e-6, kind, xq=xq, xs=xsc), COPIES, 50)
+        out["decode_us"][f"M={M},K={K}"] = round(us, 3)
+        del xs_in
+    return out
+
+
+def hbm_peak():
+    """(GB/s, source): the measured copy bandwidth, else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured hbm_gbs (copy, burst) of MEASURED_PEAKS.json"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback 6.8 TB/s"
+
+
 def progress(msg: str) -> None:
     if os.environ.get("FP8BS_BENCH_VERBOSE"):
         print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
@@ -450,8 +527,13 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     fb.build()
     fb.lib()
-    desc, calls = workload_plan(args.workload)
     stream = torch.cuda.Stream(device=dev)
+    if args.producer_only:
+        if rank == 0:
+            line = {"producer_rmsnorm_quant": producer_table(fb, torch, dev, stream, hbm_peak()[0])}
+            print(json.dumps(line), flush=True)
+        return 0
+    desc, calls = workload_plan(args.workload)
     step_bytes = sum(algorithmic_bytes(M, N, K, kind) for (M, N, K, kind, _) in calls)
     pdl = not args.no_pdl
     progress("building the step (weights, graph)")
@@ -489,12 +571,12 @@ def run_gpu(args):
         progress("per-M table, two-launch path")
         per_m_two = per_m_table(fb, torch, dev, stream, pdl, two_launch=True)
 
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak = float(json.load(f)["hbm_gbs"])
-        peak_src = "measured hbm_gbs (copy, burst) of MEASURED_PEAKS.json"
-    except (OSError, ValueError, KeyError):
-        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+    peak, peak_src = hbm_peak()
+
+    producer = None
+    if rank == 0 and not args.no_producer:
+        progress("RMSNorm + quant producer")
+        producer = producer_table(fb, torch, dev, stream, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -513,6 +595,7 @@ def run_gpu(args):
                        "pdl": pdl},
             "per_m_us_and_GBps": per_m,
             "per_m_two_launch_us_and_GBps": per_m_two,
+            "producer_rmsnorm_quant": producer,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),
                          "peak_source": peak_src, "kernel": "fused_quant_gemm_kernel",
@@ -542,6 +625,10 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-m", action="store_true")
+    ap.add_argument("--no-producer", action="store_true",
+                    help="skip the RMSNorm + quant producer's table")
+    ap.add_argument("--producer-only", action="store_true",
+                    help="time only the RMSNorm + quant producer and print its table")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain launches instead of programmatic dependent launch")
     ap.add_argument("--no-graph", action="store_true",

@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
             "fp8bs_version": ([], ci),
             "fp8bs_encode_e4m3": ([vp, i64, vp, vp], ci),
             "fp8bs_quant": ([vp, i64, i64, i64, ci, vp, vp, vp], ci),
+            "fp8bs_rmsnorm_quant": ([vp, i64, i64, i64, vp, ctypes.c_float, ci, vp, vp, vp, i64, vp], ci),
             "fp8bs_quant_weight": ([vp, i64, i64, i64, ci, vp, vp, vp], ci),
             "fp8bs_packed_weight_bytes": ([i64, i64, ci], sz),
             "fp8bs_prepack_weight": ([vp, i64, vp, i64, i64, ci, vp, sz, vp], ci),
@@ -168,6 +169,34 @@ def fp8bs_quant(x: torch.Tensor, scale_kind: int = FP8BS_SCALE_F32, xq: torch.Te
                            _stream(stream))
     _check(rc, "fp8bs_quant")
     return xq, xs
+
+
+def fp8bs_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+                        scale_kind: int = FP8BS_SCALE_F32, xq: torch.Tensor | None = None,
+                        xs: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                        want_y: bool = False, stream=None):
+    """RMSNorm of bf16 x [M, K] with bf16 weight gamma [K], then the 1x128 quant.
+
+    Returns (xq uint8 [M, K], xs [M, K/128], y bf16 [M, K] or None); y is
+    written when given or when want_y."""
+    _require_cuda(x, gamma)
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert gamma.dtype == torch.bfloat16 and gamma.dim() == 1 and gamma.is_contiguous()
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if xs is None:
+        xs = torch.empty((M, K // 128), dtype=_scale_dtype(scale_kind), device=x.device)
+    if y is None and want_y:
+        y = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    if y is not None:
+        assert y.dtype == torch.bfloat16 and y.dim() == 2 and y.stride(1) == 1
+    rc = lib().fp8bs_rmsnorm_quant(_ptr(x), M, K, x.stride(0), _ptr(gamma), float(eps),
+                                   int(scale_kind), _ptr(xq), _ptr(xs),
+                                   _ptr(y) if y is not None else None,
+                                   y.stride(0) if y is not None else 0, _stream(stream))
+    _check(rc, "fp8bs_rmsnorm_quant")
+    return xq, xs, y
 
 
 def fp8bs_quant_weight(w: torch.Tensor, scale_kind: int = FP8BS_SCALE_F32, stream=None):

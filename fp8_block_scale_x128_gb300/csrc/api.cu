@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "producer.cuh"
 
 namespace {
 
@@ -127,6 +128,18 @@ int fp8bs_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int scale_
     return status_of(launch_quant(x, M, K, ldx, scale_kind, xq, xs, as_stream(stream)));
 }
 
+int fp8bs_rmsnorm_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint16_t* gamma, float eps,
+                        int scale_kind, uint8_t* xq, void* xs, uint16_t* y, int64_t ldy, void* stream) {
+    if (!kind_ok(scale_kind) || !(eps >= 0.0f) || !(eps <= 3.4e38f)) return FP8BS_ERR_ARG;
+    if (M < 0 || K < kTile || K % kTile != 0 || K > FP8BS_RMSNORM_MAX_K || M > kMaxDim) return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !gamma || !xq || !xs) return FP8BS_ERR_ARG;
+    if (ldx < K || (y && ldy < K)) return FP8BS_ERR_ARG;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(gamma, 16) || !aligned(xq, 8) ||
+        (scale_kind == FP8BS_SCALE_F32 && !aligned(xs, 4)) || (y && (!aligned(y, 16) || ldy % 8 != 0)))
+        return FP8BS_ERR_ALIGN;
+    return status_of(launch_rmsnorm_quant(x, M, K, ldx, gamma, eps, scale_kind, xq, xs, y, ldy, as_stream(stream)));
+}
 int fp8bs_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int scale_kind, uint8_t* wq,
                        void* ws, void* stream) {
     if (!kind_ok(scale_kind)) return FP8BS_ERR_ARG;

@@ -90,7 +90,7 @@ int fp8bs_version(void);
  *         16-byte aligned.
  *   M   : rows, M >= 0 (0 enqueues nothing and returns FP8BS_OK).
  *   K   : multiple of 128, K >= 128.
- *   xq  : e4m3fn codes [M, K], row stride K (4-byte aligned).
+ *   xq  : e4m3fn codes [M, K], row stride K (8-byte aligned).
  *   xs  : [M, K/128]: fp32 (kind F32, 4-byte aligned) or e8m0 bytes (UE8M0).
  * Per group: amax = max |x| (fp32); F32: s = amax / 448 (IEEE fp32 division);
  * UE8M0: s = smallest power of two >= fp32(amax / 448), exponent clamped to
@@ -99,6 +99,36 @@ int fp8bs_version(void);
  * Errors: FP8BS_ERR_ARG, FP8BS_ERR_SHAPE, FP8BS_ERR_ALIGN, FP8BS_ERR_CUDA. */
 int fp8bs_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int scale_kind,
                 uint8_t* xq, void* xs, void* stream);
+
+/* Largest K of fp8bs_rmsnorm_quant (the row stays in registers). */
+#define FP8BS_RMSNORM_MAX_K 16384
+
+/* Fused RMSNorm + 1x128 quant: the producer of [P4] "Modifications" (the
+ * input_norm / q_norm kernels emit the GEMM's activation scales themselves,
+ * so the quant adds no launch).  Its codes and scales feed
+ * fp8bs_gemm_prequant.  Per row m, in fp32:
+ *   r = 1 / sqrt(sum_k x[m,k]^2 / K + eps)   (IEEE division and square root;
+ *                                             r = 0 when the sum and eps are 0)
+ *   y[m,k] = bf16_rn((x[m,k] * r) * gamma[k])
+ * then y is quantised exactly as fp8bs_quant quantises a bf16 input, so the
+ * bytes equal fp8bs_quant applied to the y this call writes.
+ *   x     : bf16 [M, K], row stride ldx elements; x and ldx*2 bytes 16-byte
+ *           aligned.
+ *   M     : rows, M >= 0 (0 enqueues nothing and returns FP8BS_OK).
+ *   K     : multiple of 128, 128 <= K <= FP8BS_RMSNORM_MAX_K.
+ *   gamma : bf16 [K] RMSNorm weight, 16-byte aligned.
+ *   eps   : finite, >= 0.
+ *   xq    : e4m3fn codes [M, K], row stride K (8-byte aligned).
+ *   xs    : [M, K/128]: fp32 (kind F32, 4-byte aligned) or e8m0 bytes (UE8M0).
+ *   y     : optional (NULL to skip) bf16 [M, K] normalised rows, row stride ldy
+ *           elements; y and ldy*2 bytes 16-byte aligned.
+ * The sum of squares is reduced in a fixed order: repeated calls give the same
+ * bytes.  All buffers are the caller's; nothing is allocated or synchronised.
+ * Errors: FP8BS_ERR_ARG (kind, eps, null pointer, ldx or ldy < K),
+ * FP8BS_ERR_SHAPE, FP8BS_ERR_ALIGN, FP8BS_ERR_CUDA. */
+int fp8bs_rmsnorm_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                        const uint16_t* gamma, float eps, int scale_kind, uint8_t* xq,
+                        void* xs, uint16_t* y, int64_t ldy, void* stream);
 
 /* Quantise an fp32 weight in 128x128 blocks (the offline producer of the
  * [N/128, K/128] weight scale of [P1] "Modifications"; with UE8M0 each block

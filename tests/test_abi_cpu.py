@@ -172,6 +172,30 @@ def test_quant_host_checks(L):
     assert q(P, 2, 4096, 4096, 0, P, P + 2, STREAM) == ALIGN
 
 
+def test_rmsnorm_quant_host_checks(L):
+    r = L.fp8bs_rmsnorm_quant
+    nan = float("nan")
+    # x, M, K, ldx, gamma, eps, kind, xq, xs, y, ldy, stream
+    assert r(P, 2, 4096, 4096, P, 1e-6, 2, P, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4096, 4096, P, -1e-6, 0, P, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4096, 4096, P, nan, 0, P, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4000, 4000, P, 1e-6, 0, P, P, None, 0, STREAM) == SHAPE
+    assert r(P, 2, 16384 + 128, 16512, P, 1e-6, 0, P, P, None, 0, STREAM) == SHAPE
+    assert r(P, -1, 4096, 4096, P, 1e-6, 0, P, P, None, 0, STREAM) == SHAPE
+    assert r(P, 0, 4096, 4096, None, 1e-6, 0, None, None, None, 0, STREAM) == OK
+    assert r(P, 2, 4096, 4096, None, 1e-6, 0, P, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, None, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4096, 2048, P, 1e-6, 0, P, P, None, 0, STREAM) == ARG
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P, P, 2048, STREAM) == ARG
+    assert r(P + 8, 2, 4096, 4096, P, 1e-6, 0, P, P, None, 0, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4100, P, 1e-6, 0, P, P, None, 0, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4096, P + 2, 1e-6, 0, P, P, None, 0, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, P + 4, P, None, 0, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P + 2, None, 0, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P, P + 8, 4096, STREAM) == ALIGN
+    assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P, P, 4100, STREAM) == ALIGN
+
+
 def test_prepack_and_weight_quant_host_checks(L):
     pp = L.fp8bs_prepack_weight
     assert pp(P, 4096, P, 5120, 4096, 5, P, 1 << 30, STREAM) == ARG
