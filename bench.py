@@ -412,11 +412,14 @@ def time_steps(torch, step: Step, steps: int, warmup: int, world: int, dev) -> f
     return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
 
-def per_m_table(fb, torch, dev, stream, pdl, two_launch=False):
+M_ABOVE_32 = [33, 48, 64]
+
+
+def per_m_table(fb, torch, dev, stream, pdl, two_launch=False, ms=None):
     """us/call and GB/s per M at N=5120 K=4096 (graph of 24 rotated calls);
     two_launch: fp8bs_quant + fp8bs_gemm_prequant per call instead."""
     out = {}
-    for M in M_SWEEP:
+    for M in (M_SWEEP if ms is None else ms):
         st = Step(fb, torch, [(M, 5120, 4096, 0, c) for c in range(COPIES)], dev, stream, pdl=pdl,
                   two_launch=two_launch)
         progress(f"per-M step M={M}")
@@ -564,12 +567,16 @@ def run_gpu(args):
     del st_io
     torch.cuda.empty_cache()
 
-    per_m = per_m_two = None
+    per_m = per_m_two = above_32 = None
     if args.workload == "msweep" and rank == 0 and not args.no_per_m:
         progress("per-M table")
         per_m = per_m_table(fb, torch, dev, stream, pdl)
         progress("per-M table, two-launch path")
         per_m_two = per_m_table(fb, torch, dev, stream, pdl, two_launch=True)
+        progress("33..64 tokens (64-token tile)")
+        above_32 = {"fused": per_m_table(fb, torch, dev, stream, pdl, ms=M_ABOVE_32),
+                    "two_launch": per_m_table(fb, torch, dev, stream, pdl, two_launch=True,
+                                              ms=M_ABOVE_32)}
 
     peak, peak_src = hbm_peak()
 
@@ -595,6 +602,7 @@ def run_gpu(args):
                        "pdl": pdl},
             "per_m_us_and_GBps": per_m,
             "per_m_two_launch_us_and_GBps": per_m_two,
+            "m_above_32_us_and_GBps": above_32,
             "producer_rmsnorm_quant": producer,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),

@@ -24,7 +24,7 @@ import torch
 
 FP8BS_SCALE_F32 = 0
 FP8BS_SCALE_UE8M0 = 1
-FP8BS_MAX_M = 32
+FP8BS_MAX_M = 64
 FP8BS_FLAG_PDL = 1
 FP8BS_STATIC_MAX_K = 16384
 FP8BS_STATIC_MAX_SMS = 160
@@ -261,7 +261,7 @@ def fp8bs_gemm_fused(x: torch.Tensor, packed: torch.Tensor, N: int, K: int,
                      workspace: torch.Tensor | None = None, xq_out: torch.Tensor | None = None,
                      xs_out: torch.Tensor | None = None, pdl: bool = False,
                      stream=None) -> torch.Tensor:
-    """Y = bf16(quant(x) . W^T) for bf16 x [M <= 32, K] and a packed weight.
+    """Y = bf16(quant(x) . W^T) for bf16 x [M <= 64, K] and a packed weight.
 
     pdl=True launches with programmatic dependent launch (FP8BS_FLAG_PDL); use
     it only when the work just before this call on the stream does not write

@@ -58,7 +58,7 @@ size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_c
 // a caller's workspace for FP8BS_STATIC_MAX_SMS CTAs and K up to
 // FP8BS_STATIC_MAX_K.
 constexpr size_t kStaticScratchBytes = ws_total_bytes(FP8BS_STATIC_MAX_SMS, FP8BS_STATIC_MAX_K);
-static_assert(kStaticScratchBytes == 6344960, "fp8bs.h states the scratch size");
+static_assert(kStaticScratchBytes == 7426304, "fp8bs.h states the scratch size");
 
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 

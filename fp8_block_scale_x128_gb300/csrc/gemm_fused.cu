@@ -71,7 +71,6 @@ constexpr int kQuantThreads = 160;  // warps 2 and 4-7
 constexpr int kQuantHalfWarps = kQuantThreads / 16;
 constexpr int kLocalMaxM = 6;  // up to this many tokens every CTA quantises its own groups
 constexpr int kAccStages = 4;
-constexpr uint32_t kMaxSmemPerCta = 112 * 1024;  // two CTAs per SM
 
 // Where a CTA's activation codes come from.
 enum : int {
@@ -80,10 +79,14 @@ enum : int {
     kSrcInput = 2,     // codes and scales given by the caller (the two-launch path)
 };
 
+// MPAD 16 and 32: two CTAs per SM (the next call's CTAs start while this
+// call's finish); MPAD 64: one CTA per SM with a deeper weight ring.
 template <int MPAD, int SRC>
 struct Cfg {
-    static constexpr int kUnits = MPAD == 16 ? kMaxUnitsM16 : kMaxUnitsM32;
-    static constexpr int kStages = MPAD == 16 ? 5 : 4;
+    static constexpr int kCtasPerSm = MPAD == 64 ? 1 : 2;
+    static constexpr uint32_t kMaxSmem = MPAD == 64 ? 227 * 1024 : 112 * 1024;
+    static constexpr int kUnits = MPAD == 16 ? kMaxUnitsM16 : (MPAD == 32 ? kMaxUnitsM32 : kMaxUnitsM64);
+    static constexpr int kStages = MPAD == 16 ? 5 : (MPAD == 32 ? 4 : 8);
     static constexpr uint32_t kBBytes = MPAD * 128;  // activation operand of one unit
     static constexpr uint32_t kTmemCols = kAccStages * MPAD;
     static constexpr uint32_t kRingBytes = kStages * kTileBytes;
@@ -101,7 +104,8 @@ struct Cfg {
     static constexpr int kGroupsPerHw = (kUnits * kLocalMaxM + kQuantHalfWarps - 1) / kQuantHalfWarps;
     // exchange: groups (unit, token) per quantising thread
     static constexpr int kGroupsPerThread = (kUnits * MPAD + kQuantThreads - 1) / kQuantThreads;
-    static_assert(kSmem <= kMaxSmemPerCta, "shared memory per CTA");
+    static_assert(kSmem <= kMaxSmem, "shared memory per CTA");
+    static_assert(MPAD == 16 || MPAD == 32 || MPAD == 64, "token tile");
     static_assert(kBBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
 };
@@ -120,7 +124,7 @@ struct Params {
     uint32_t* err;
     uint32_t* gen;            // epoch words
     uint32_t* pflag;          // partial flags [CTA][4 epilogue warps]
-    uint64_t* slots;          // partial slots [CTA][32 columns][128 rows]: tagged words or fp32
+    uint64_t* slots;          // partial slots, 32 KB per CTA: [32 cols][128 rows] tagged or [64][128] fp32
     uint8_t* act;             // activation records [K/128][kKbRecBytes]
     uint8_t* xq_out;
     void* xs_out;
@@ -383,7 +387,8 @@ __device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t
 }
 
 template <int MPAD, int KIND, int SRC, bool TAGGED>
-__global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
+    fused_quant_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MPAD, SRC>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -751,20 +756,19 @@ __global__ void __launch_bounds__(kThreads, 2) fused_quant_gemm_kernel(const __g
                 if (__shfl_sync(0xFFFFFFFFu, done, 0) == 0) break;
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
-                uint32_t r0[16], r1[16];
-                ptx::tmem_ld_32x32b_x16(taddr, r0);
-                if constexpr (MPAD == 32) ptx::tmem_ld_32x32b_x16(taddr + 16, r1);
+                uint32_t r[MPAD / 16][16];
+#pragma unroll
+                for (int h = 0; h < MPAD / 16; ++h) ptx::tmem_ld_32x32b_x16(taddr + 16 * h, r[h]);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&acce[a]);  // this warp is done with the stage
                 const float sw = sWs[i];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) acc[m] = fmaf(__uint_as_float(r0[m]), sXs[i * MPAD + m] * sw, acc[m]);
-                if constexpr (MPAD == 32) {
+                for (int h = 0; h < MPAD / 16; ++h) {
 #pragma unroll
                     for (int m = 0; m < 16; ++m)
-                        acc[16 + m] = fmaf(__uint_as_float(r1[m]), sXs[i * MPAD + 16 + m] * sw, acc[16 + m]);
+                        acc[16 * h + m] = fmaf(__uint_as_float(r[h][m]), sXs[i * MPAD + 16 * h + m] * sw, acc[16 * h + m]);
                 }
                 if (++kb == KB || i == cnt - 1) {  // the tile ends here, or this CTA's range does
                     // whole tile in this CTA -> 0; this CTA started inside the tile
@@ -872,12 +876,14 @@ cudaError_t launch_kind(const Params& p, const FusedArgs& a, cudaStream_t stream
     if (a.xq_in) {
         if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcInput, true>(p, a, stream);
         if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput, false>(p, a, stream);
-        return launch_chunks<32, KIND, kSrcInput, false>(p, a, stream);
+        if (a.M <= 32) return launch_chunks<32, KIND, kSrcInput, false>(p, a, stream);
+        return launch_chunks<64, KIND, kSrcInput, false>(p, a, stream);
     }
     if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, kSrcLocal, true>(p, a, stream);
     if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcExchange, true>(p, a, stream);
     if (a.M <= 16) return launch_chunks<16, KIND, kSrcExchange, false>(p, a, stream);
-    return launch_chunks<32, KIND, kSrcExchange, false>(p, a, stream);
+    if (a.M <= 32) return launch_chunks<32, KIND, kSrcExchange, false>(p, a, stream);
+    return launch_chunks<64, KIND, kSrcExchange, false>(p, a, stream);
 }
 
 }  // namespace
@@ -911,7 +917,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
 bool fused_shape_supported(int64_t N, int64_t K, int sm_count) {
     if (N < kTile || K < kTile || N % kTile != 0 || K % kTile != 0) return false;
     if (sm_count < 1 || sm_count > kMaxCtas) return false;
-    return K / kTile <= static_cast<int64_t>(sm_count) * kMaxUnitsM32;
+    constexpr int64_t kMinUnits = kMaxUnitsM32 < kMaxUnitsM64 ? kMaxUnitsM32 : kMaxUnitsM64;
+    return K / kTile <= static_cast<int64_t>(sm_count) * kMinUnits;
 }
 
 }  // namespace fp8bs

@@ -47,18 +47,18 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
 //   [0, 256)                  device error word
 //   [256, +4 KB)              epoch words, one per possible CTA index
 //   [4352, +16 KB)            partial flags, one per (CTA index, epilogue warp)
-//   then sm_count x 32 KB     split-K partial slots, [32 columns][128 rows] of
-//                             tagged words or (first 16 KB) of fp32
-//   then K/128 x 8448 B       one record per K block of the activations:
-//                             32 scale words, 32 rows x 32 words of 4 codes
+//   then sm_count x 32 KB     split-K partial slots: [32 columns][128 rows] of
+//                             tagged words, or [64 columns][128 rows] of fp32
+//   then K/128 x 16896 B      one record per K block of the activations:
+//                             64 scale words, 64 rows x 32 words of 4 codes
 constexpr size_t kWsErrorBytes = 256;
 constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
 constexpr size_t kWsGenBytes = kMaxCtas * sizeof(uint32_t);
 constexpr size_t kWsPflagBytes = kMaxCtas * 4 * sizeof(uint32_t);
 constexpr size_t kSlotBytes = 32 * 128 * sizeof(uint64_t);
 constexpr size_t kKbRecScales = 0;                       // within a K-block record
-constexpr size_t kKbRecCodes = 32 * sizeof(uint64_t);
-constexpr size_t kKbRecBytes = kKbRecCodes + 32 * 32 * sizeof(uint64_t);
+constexpr size_t kKbRecCodes = 64 * sizeof(uint64_t);
+constexpr size_t kKbRecBytes = kKbRecCodes + 64 * 32 * sizeof(uint64_t);
 
 __host__ __device__ constexpr size_t ws_gen_offset() { return kWsErrorBytes; }
 __host__ __device__ constexpr size_t ws_pflag_offset() { return kWsErrorBytes + kWsGenBytes; }
@@ -73,6 +73,7 @@ __host__ __device__ constexpr size_t ws_total_bytes(int sm_count, int64_t K) {
 // Units of work (128x128 weight tiles) one CTA of the fused kernel owns at most.
 constexpr int kMaxUnitsM16 = 12;
 constexpr int kMaxUnitsM32 = 10;
+constexpr int kMaxUnitsM64 = 10;
 
 // Device error word: 0, or the negated status of the first fault.
 __device__ inline void record_error(uint32_t* err, int status) {

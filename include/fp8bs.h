@@ -70,9 +70,11 @@ typedef enum {
     FP8BS_ERR_DEVICE = -8,     /* device: another device-side check failed */
 } fp8bs_status;
 
-/* Largest token count of the fused GEMM ([P1] "Motivation": one launch for
- * M <= 32; larger inputs keep the library path). */
-#define FP8BS_MAX_M 32
+/* Largest token count of the fused GEMM.  [P1] "Motivation" fuses up to 32
+ * tokens and keeps the library path above; [P2] "Modifications" raises the
+ * small-M MoE kernel's cap to 48 tokens at TP8, where the library path slows.
+ * Here 33..64 tokens run with a 64-token tile (one CTA per SM). */
+#define FP8BS_MAX_M 64
 
 /* Text for a status code.  Never NULL; static storage. */
 const char* fp8bs_status_string(int status);
@@ -177,7 +179,7 @@ int fp8bs_prepack_weight(const uint8_t* wq, int64_t ldw, const void* ws, int64_t
 
 /* ------------------------------------------------------------------------ */
 /* Fused quant + block-scale GEMM ([P1] "Modifications": one launch per      */
-/* linear at M <= 32)                                                        */
+/* linear at M <= 32; here up to FP8BS_MAX_M)                                */
 /* ------------------------------------------------------------------------ */
 
 /* Flags of fp8bs_gemm_fused. */
@@ -194,7 +196,7 @@ enum {
 /* Workspace bytes the fused GEMM needs for an N x K weight on a device with
  * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
  * CUDA device): a 256-byte error word, 4 KB of epoch words, 16 KB of
- * split-K flags, one 32 KB split-K slot per multiprocessor and 8.25 KB per
+ * split-K flags, one 32 KB split-K slot per multiprocessor and 16.5 KB per
  * 128 columns of K for the quantised activations the CTAs exchange.  The size
  * depends on K and sm_count only and every region sits at a place that
  * depends on sm_count only, so a workspace sized for the largest K serves
@@ -266,7 +268,7 @@ int fp8bs_check_error(void* workspace, void* stream);
 #define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */
 
 /* fp8bs_gemm_fused without a workspace argument: the scratch lives in one
- * fixed device array inside this library (6,344,960 bytes per device,
+ * fixed device array inside this library (7,426,304 bytes per device,
  * sized for FP8BS_STATIC_MAX_SMS CTAs and K up to FP8BS_STATIC_MAX_K), so the
  * call allocates no device memory, ever.  It is meant for callers that cannot
  * allocate or own device memory: an operator plugged into a runtime whose

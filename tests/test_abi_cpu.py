@@ -52,7 +52,7 @@ def test_packed_weight_bytes(L):
 
 def test_workspace_bytes_for_explicit_sm_count(L):
     def expect(K, sm):
-        return 256 + 4096 + 16384 + sm * 32 * 128 * 8 + (K // 128) * (32 * 8 + 32 * 32 * 8)
+        return 256 + 4096 + 16384 + sm * 32 * 128 * 8 + (K // 128) * (64 * 8 + 64 * 32 * 8)
     assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == expect(4096, 152)
     assert fb.fp8bs_workspace_bytes(128, 128, 152) == expect(128, 152)
     # independent of N
@@ -72,7 +72,7 @@ def gemm(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K=4096, 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(kind=2), ARG),
-    (dict(M=33), SHAPE),
+    (dict(M=65), SHAPE),
     (dict(M=-1), SHAPE),
     (dict(N=5000), SHAPE),
     (dict(K=4000, ldx=4000), SHAPE),
@@ -110,7 +110,7 @@ def gemm_static(L, x=P, M=4, ldx=4096, packed=P, packed_bytes=1 << 30, N=5120, K
 @pytest.mark.parametrize("kw,status", [
     (dict(kind=2), ARG),
     (dict(flags=2), ARG),
-    (dict(M=33), SHAPE),
+    (dict(M=65), SHAPE),
     (dict(N=5000), SHAPE),
     (dict(x=None), ARG),
     (dict(packed=None), ARG),
@@ -139,7 +139,7 @@ def gemm_prequant(L, xq=P, M=4, ldxq=4096, xs=P, packed=P, packed_bytes=1 << 30,
 @pytest.mark.parametrize("kw,status", [
     (dict(kind=3), ARG),
     (dict(flags=2), ARG),
-    (dict(M=33), SHAPE),
+    (dict(M=65), SHAPE),
     (dict(K=4000, ldxq=4000), SHAPE),
     (dict(xq=None), ARG),
     (dict(xs=None), ARG),

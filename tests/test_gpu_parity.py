@@ -249,7 +249,17 @@ def test_fused_ue8m0_shapes(dev, oracle_mod, N, K, M):
     run_fused(oracle_mod, dev, M, N, K, UE8, seed=3000 + M + N // 128)
 
 
-@pytest.mark.parametrize("M,kind", [(4, F32), (9, F32), (17, F32), (32, UE8)])
+@pytest.mark.parametrize("M", [33, 40, 48, 64])
+@pytest.mark.parametrize("N,K,kind", [(384, 640, F32), (5120, 4096, F32), (4096, 2048, F32),
+                                      (7168, 2048, UE8), (1536, 7168, UE8), (4096, 4096, UE8)])
+def test_fused_above_32_tokens(dev, oracle_mod, N, K, kind, M):
+    # 33..64 tokens: the 64-token tile (one CTA per SM, deeper weight ring)
+    # with the activation exchange and flagged split-K partials, quant bytes
+    # included
+    run_fused(oracle_mod, dev, M, N, K, kind, seed=8000 + M + N // 128 + K // 128)
+
+
+@pytest.mark.parametrize("M,kind", [(4, F32), (9, F32), (17, F32), (32, UE8), (64, F32)])
 def test_fused_weight_larger_than_one_launch(dev, oracle_mod, M, kind):
     # 8192 units: more than one CTA per SM can hold, so the call runs several
     # launches of whole 128-row slices
@@ -258,7 +268,8 @@ def test_fused_weight_larger_than_one_launch(dev, oracle_mod, M, kind):
 
 @pytest.mark.parametrize("kind", [F32, UE8])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 384, 640), (9, 1024, 1024), (17, 640, 2048),
-                                   (32, 5120, 4096), (3, 5120, 4096), (16, 4096, 2048)])
+                                   (32, 5120, 4096), (3, 5120, 4096), (16, 4096, 2048),
+                                   (48, 5120, 4096), (64, 1536, 7168)])
 def test_prequant_gemm_against_oracle(dev, oracle_mod, kind, M, N, K):
     # the second launch of the two-launch path, fed the oracle's quantised x
     x = synth.x_bf16(M, K, seed=6000 + M + K // 128)
@@ -274,7 +285,7 @@ def test_prequant_gemm_against_oracle(dev, oracle_mod, kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", [F32, UE8])
-@pytest.mark.parametrize("M", [1, 6, 7, 12, 13, 16, 17, 32])
+@pytest.mark.parametrize("M", [1, 6, 7, 12, 13, 16, 17, 32, 33, 64])
 def test_two_launch_path_is_bit_identical_to_fused(dev, kind, M):
     # fp8bs_quant + fp8bs_gemm_prequant runs the same MMAs, rescale and split-K
     # order as the fused call on the same x
@@ -454,7 +465,7 @@ def test_fused_rejects_mismatched_packed_weight(dev, oracle_mod):
 
 
 def test_fused_host_errors_raise(dev, oracle_mod):
-    M, N, K = 33, 256, 512
+    M, N, K = 65, 256, 512
     xd = torch.zeros((M, K), dtype=torch.bfloat16, device=dev)
     packed = torch.zeros(fb.fp8bs_packed_weight_bytes(N, K, F32), dtype=torch.uint8, device=dev)
     with pytest.raises(fb.Fp8bsError) as e:
