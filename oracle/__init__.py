@@ -10,7 +10,8 @@ from these pages:
   [N/128, K/128] fp32 weight scales, x_scale * w_scale in fp32 per K block.
 * "[AMD] gfx950 small-batch MoE: expert-count gate for the small sort and FP8
   block-scale small-M kernel", section "Modifications" -- float8_e4m3fn and
-  the 128x128 block scale applied to each partial sum.
+  the 128x128 block scale applied to each partial sum (also the w13 / w2 of
+  its small-M MoE layer).
 * "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense 128x128 fp8
   linears (6/8)", "Motivation" / "Modifications" -- power-of-two (e8m0)
   weight scales and ue8m0 activation scales, emitted by the fused
@@ -91,6 +92,9 @@ def _load():
         lib.oracle_rmsnorm_quant.argtypes = [vp, i64, i64, i64, vp, c.c_double, c.c_int, vp, vp,
                                              vp]
         lib.oracle_rmsnorm_quant.restype = c.c_int
+        lib.oracle_moe_w8a16.argtypes = [vp, i64, i64, vp, vp, i64, vp, vp, vp, vp, i64, i64, vp,
+                                         vp]
+        lib.oracle_moe_w8a16.restype = c.c_int
         _lib = lib
         return lib
 
@@ -249,6 +253,36 @@ def rmsnorm_quant(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float, kind: 
     if rc:
         raise ValueError("oracle_rmsnorm_quant rejected its arguments")
     return y, xq, xs
+
+
+def moe_w8a16(x_bf16, ids, topk_w, w13, s13, w2, s2, want_f64: bool = False):
+    """Small-M FP8 block-scale MoE layer (bf16 activations, e4m3 weights with
+    128x128 fp32 block scales).  x [M, H] bf16 bits; ids int32 [M, S]; topk_w
+    fp32 [M, S]; w13 uint8 [E, 2I, H]; s13 fp32 [E, 2I/128, H/128]; w2 uint8
+    [E, H, I]; s2 fp32 [E, H/128, I/128].  Returns y bf16 bits [M, H] (and the
+    fp64 values before rounding)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    tw = np.ascontiguousarray(topk_w, dtype=np.float32)
+    w13 = np.ascontiguousarray(w13, dtype=np.uint8)
+    w2 = np.ascontiguousarray(w2, dtype=np.uint8)
+    s13 = np.ascontiguousarray(s13, dtype=np.float32)
+    s2 = np.ascontiguousarray(s2, dtype=np.float32)
+    M, H = x.shape
+    S = ids.shape[1]
+    E, I2, _ = w13.shape
+    I = I2 // 2
+    assert ids.shape == (M, S) and tw.shape == (M, S) and w13.shape == (E, 2 * I, H)
+    assert w2.shape == (E, H, I) and s13.shape == (E, 2 * I // 128, H // 128)
+    assert s2.shape == (E, H // 128, I // 128)
+    y = np.empty((M, H), dtype=np.uint16)
+    y64 = np.empty((M, H), dtype=np.float64) if want_f64 else None
+    rc = _load().oracle_moe_w8a16(_ptr(x), M, H, _ptr(ids), _ptr(tw), S, _ptr(w13), _ptr(s13),
+                                  _ptr(w2), _ptr(s2), E, I, _ptr(y),
+                                  _ptr(y64) if want_f64 else None)
+    if rc:
+        raise ValueError("oracle_moe_w8a16 rejected its arguments")
+    return (y, y64) if want_f64 else y
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:

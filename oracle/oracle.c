@@ -18,7 +18,7 @@
  *   [P2] "[AMD] gfx950 small-batch MoE: expert-count gate for the small sort and
  *        FP8 block-scale small-M kernel", section "Modifications": names the fp8
  *        format float8_e4m3fn and the 128x128 fp32 block scale applied to each
- *        partial sum.
+ *        partial sum, for the w13 / w2 weights of its small-M MoE layer.
  *   [P4] "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense 128x128 fp8
  *        linears (6/8)", sections "Motivation" and "Modifications": power-of-two
  *        128x128 weight scales stored as one e8m0 byte per block, and ue8m0
@@ -38,6 +38,9 @@
  *   - the fp64 result is rounded straight to bf16, nearest-even.
  *   - the RMSNorm producer normalises each whole row, x * gamma /
  *     sqrt(mean x^2 + eps), rounds that to bf16 and quantises the bf16 values.
+ *   - the MoE layer: gate rows over up rows in w13, a = bf16(silu(gate) * up),
+ *     y = bf16(sum over slots of weight * (a . w2^T)) (details at
+ *     oracle_moe_w8a16).
  *
  * Build: gcc -O2 -fPIC -shared -ffp-contract=off -pthread (no fast-math: every
  * fp32 operation below must be the IEEE one).
@@ -417,4 +420,85 @@ int oracle_rmsnorm_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
     int rc = oracle_rmsnorm(x, M, K, ldx, gamma, eps, NULL, y);
     if (rc) return rc;
     return oracle_quant_1x128(y, M, K, K, kind, xq, xs);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Small-M FP8 block-scale MoE [P2 "Modifications": float8_e4m3fn w13 / w2   */
+/* with contiguous [128 x 128] fp32 block scales, each block's scale applied  */
+/* to its partial sum; bf16 activations; routing given per token as S slots]  */
+/* ------------------------------------------------------------------------- */
+
+/* Readings (the page names the weights and the scale rule, not the layer):
+ *   - w13[e] stacks the gate rows (0 .. I-1) over the up rows (I .. 2I-1),
+ *     each [2I, H] row-major; w2[e] is [H, I]; scales s13 [E][2I/128][H/128]
+ *     and s2 [E][H/128][I/128], fp32;
+ *   - h = x . w13[e]^T with, per 128-wide K block, the block's partial sum
+ *     times its scale (x in bf16, weights decoded exactly);
+ *   - a = silu(h_gate) * h_up with silu(g) = g / (1 + exp(-g)), rounded to
+ *     bf16: the intermediate activation the down projection reads;
+ *   - o = a . w2[e]^T, the same block-scale rule;
+ *   - y[m] = bf16(sum over the token's S slots of topk_w * o), with every slot
+ *     summed (a token routed twice to one expert counts twice).
+ * Everything else in fp64.  x: bf16 [M, H]; ids: int32 [M, S] in [0, E);
+ * w: fp32 [M, S]; y: bf16 [M, H] (nullable); y64: fp64 [M, H] (nullable).
+ * Returns 0, or -1 on a bad shape or an expert id out of range. */
+int oracle_moe_w8a16(const uint16_t* x, int64_t M, int64_t H, const int32_t* ids,
+                     const float* w, int64_t S, const uint8_t* w13, const float* s13,
+                     const uint8_t* w2, const float* s2, int64_t E, int64_t I, uint16_t* y,
+                     double* y64) {
+    if (M < 0 || S < 1 || E < 1 || H <= 0 || I <= 0 || H % 128 != 0 || I % 128 != 0) return -1;
+    for (int64_t p = 0; p < M * S; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return -1;
+    double table[256];
+    for (int c = 0; c < 256; ++c) table[c] = oracle_e4m3_decode((uint8_t)c);
+    const int64_t HB = H / 128, IB = I / 128;
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!h || !a || !acc || !xv) {
+        free(h); free(a); free(acc); free(xv);
+        return -1;
+    }
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < H; ++k) xv[k] = (double)oracle_bf16_to_f32(x[m * H + k]);
+        for (int64_t n = 0; n < H; ++n) acc[n] = 0.0;
+        for (int64_t s = 0; s < S; ++s) {
+            const int64_t e = ids[m * S + s];
+            const uint8_t* W13 = w13 + e * (2 * I) * H;
+            const float* S13 = s13 + e * (2 * I / 128) * HB;
+            for (int64_t j = 0; j < 2 * I; ++j) {
+                double hj = 0.0;
+                for (int64_t kb = 0; kb < HB; ++kb) {
+                    double part = 0.0;
+                    for (int64_t k = kb * 128; k < kb * 128 + 128; ++k) part += xv[k] * table[W13[j * H + k]];
+                    hj += part * (double)S13[(j / 128) * HB + kb];
+                }
+                h[j] = hj;
+            }
+            for (int64_t i = 0; i < I; ++i) {
+                const double g = h[i], u = h[I + i];
+                const double act = g / (1.0 + exp(-g)) * u;
+                a[i] = (double)oracle_bf16_to_f32(oracle_f64_to_bf16(act));
+            }
+            const uint8_t* W2 = w2 + e * H * I;
+            const float* S2 = s2 + e * HB * IB;
+            const double ws = (double)w[m * S + s];
+            for (int64_t n = 0; n < H; ++n) {
+                double o = 0.0;
+                for (int64_t ib = 0; ib < IB; ++ib) {
+                    double part = 0.0;
+                    for (int64_t i = ib * 128; i < ib * 128 + 128; ++i) part += a[i] * table[W2[n * I + i]];
+                    o += part * (double)S2[(n / 128) * IB + ib];
+                }
+                acc[n] += ws * o;
+            }
+        }
+        for (int64_t n = 0; n < H; ++n) {
+            if (y) y[m * H + n] = oracle_f64_to_bf16(acc[n]);
+            if (y64) y64[m * H + n] = acc[n];
+        }
+    }
+    free(h); free(a); free(acc); free(xv);
+    return 0;
 }

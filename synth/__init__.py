@@ -15,6 +15,10 @@ Recipes:
   W  -- fp32 [N, K]: N(0, 0.02).
   gamma -- bf16 [K], the RMSNorm weight of the producer: fp32 1 + 0.25 * N(0, 1),
         rounded to bf16 (nearest even).
+  MoE routing -- per token S slots: S-1 distinct routed experts drawn uniformly
+        from experts 0 .. E-2 with weights exp(N(0, 1)) normalised to sum 1,
+        and the shared expert E-1 in the last slot with weight 1 (Qwen3.5's
+        11 slots per token: 10 routed + 1 shared, out of 513 experts).
 Seeds: ``seed = 1000 * workload + copy`` by convention of the callers.
 """
 
@@ -63,6 +67,20 @@ def gamma_bf16(K: int, seed: int) -> np.ndarray:
     rng = _rng(seed)
     v = (np.float32(1.0) + rng.standard_normal(K, dtype=np.float32) * np.float32(GAMMA_STD))
     return f32_to_bf16_bits(v.astype(np.float32))
+
+
+def moe_routing(M: int, S: int, E: int, seed: int):
+    """(ids int32 [M, S], weights float32 [M, S]) per the routing recipe."""
+    rng = _rng(seed)
+    ids = np.empty((M, S), dtype=np.int32)
+    w = np.empty((M, S), dtype=np.float32)
+    for m in range(M):
+        ids[m, :S - 1] = rng.choice(E - 1, size=S - 1, replace=False)
+        ids[m, S - 1] = E - 1
+        g = np.exp(rng.standard_normal(S - 1)).astype(np.float64)
+        w[m, :S - 1] = (g / g.sum()).astype(np.float32)
+        w[m, S - 1] = 1.0
+    return ids, w
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:

@@ -515,3 +515,86 @@ def test_rmsnorm_quant_is_quant_of_the_rounded_norm(oracle_mod):
         assert np.array_equal(xq, q2) and np.array_equal(xsc, s2)
         if kind == 0:  # every non-zero group holds a byte of magnitude 0x7E
             assert np.all((xq.reshape(5, K // 128, 128) & 0x7F).max(axis=2) == 0x7E)
+
+
+# ---------------------------------------------------------------------------
+# Small-M FP8 block-scale MoE ("[AMD] gfx950 small-batch MoE: expert-count gate
+# for the small sort and FP8 block-scale small-M kernel", "Modifications":
+# e4m3 w13 / w2 with 128x128 fp32 block scales applied to each partial sum).
+# Reading: a = bf16(silu(gate) * up), y = bf16(sum_s topk_w * (a . w2^T)).
+# ---------------------------------------------------------------------------
+
+def _moe_inputs(oracle_mod, M, S, E, H, I, seed):
+    x = synth.x_bf16(M, H, seed=seed)
+    ids, tw = synth.moe_routing(M, S, E, seed=seed + 1)
+    w13, s13 = oracle_mod.quant_weight_128x128(synth.w_f32(E * 2 * I, H, seed=seed + 2), 0)
+    w2, s2 = oracle_mod.quant_weight_128x128(synth.w_f32(E * H, I, seed=seed + 3), 0)
+    return (x, ids, tw, w13.reshape(E, 2 * I, H), s13.reshape(E, 2 * I // 128, H // 128),
+            w2.reshape(E, H, I), s2.reshape(E, H // 128, I // 128))
+
+
+def _bf16_round_f64(oracle_mod, v):
+    return synth.bf16_bits_to_f32(oracle_mod.f64_to_bf16_array(v)).astype(np.float64)
+
+
+def test_moe_matches_dequantized_numpy_reference(oracle_mod):
+    # the blocked partial sums equal numpy's matmul of the dequantised weights
+    M, S, E, H, I = 3, 4, 5, 384, 256
+    x, ids, tw, w13, s13, w2, s2 = _moe_inputs(oracle_mod, M, S, E, H, I, seed=41)
+    _, y64 = oracle_mod.moe_w8a16(x, ids, tw, w13, s13, w2, s2, want_f64=True)
+    dec = oracle_mod.e4m3_table()
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    W13 = dec[w13] * np.repeat(np.repeat(s13.astype(np.float64), 128, axis=1), 128, axis=2)
+    W2 = dec[w2] * np.repeat(np.repeat(s2.astype(np.float64), 128, axis=1), 128, axis=2)
+    ref = np.zeros((M, H))
+    for m in range(M):
+        for s in range(S):
+            e = ids[m, s]
+            h = W13[e] @ xf[m]
+            g, u = h[:I], h[I:]
+            a = _bf16_round_f64(oracle_mod, g / (1.0 + np.exp(-g)) * u)
+            ref[m] += float(tw[m, s]) * (W2[e] @ a)
+    np.testing.assert_allclose(y64, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+
+
+def test_moe_identity_weights_give_silu_closed_form(oracle_mod):
+    # w13 = [I; I] (gate = up = x), w2 = I, scales 1: y = w * bf16(silu(x) * x)
+    H = I = 128
+    E, M, S = 1, 1, 1
+    one = 0x38  # e4m3 code of 1.0
+    w13 = np.zeros((E, 2 * I, H), np.uint8)
+    w13[0, np.arange(I), np.arange(I)] = one
+    w13[0, I + np.arange(I), np.arange(I)] = one
+    w2 = np.zeros((E, H, I), np.uint8)
+    w2[0, np.arange(H), np.arange(I)] = one
+    s13 = np.ones((E, 2, 1), np.float32)
+    s2 = np.ones((E, 1, 1), np.float32)
+    xv = np.zeros(H, np.float32)
+    xv[:4] = [1.0, -1.0, 2.0, 0.5]
+    x = synth.f32_to_bf16_bits(xv)[None, :]
+    _, y64 = oracle_mod.moe_w8a16(x, np.zeros((1, 1), np.int32), np.full((1, 1), 0.5, np.float32),
+                                  w13, s13, w2, s2, want_f64=True)
+    for k, v in enumerate([1.0, -1.0, 2.0, 0.5]):
+        act = v * v / (1.0 + math.exp(-v))
+        expect = 0.5 * float(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(np.float32([act])))[0])
+        assert y64[0, k] == pytest.approx(expect, rel=2 ** -8)
+    assert np.all(y64[0, 4:] == 0.0)
+    assert y64[0, 0] == pytest.approx(0.5 * 0.73046875, rel=1e-12)  # bf16(silu(1)) = 0.73046875
+
+
+def test_moe_is_linear_in_the_routing_weights(oracle_mod):
+    # the same expert in two slots with weights a and b equals one slot a + b;
+    # zero weights give a zero output
+    M, S, E, H, I = 2, 3, 4, 256, 128
+    x, ids, tw, w13, s13, w2, s2 = _moe_inputs(oracle_mod, M, S, E, H, I, seed=51)
+    ids2 = ids.copy()
+    ids2[:, 1] = ids2[:, 0]
+    w_split = tw.copy()
+    w_split[:, 0], w_split[:, 1] = 0.25, 0.5
+    w_one = w_split.copy()
+    w_one[:, 0], w_one[:, 1] = 0.75, 0.0
+    _, a = oracle_mod.moe_w8a16(x, ids2, w_split, w13, s13, w2, s2, want_f64=True)
+    _, b = oracle_mod.moe_w8a16(x, ids2, w_one, w13, s13, w2, s2, want_f64=True)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+    _, z = oracle_mod.moe_w8a16(x, ids, np.zeros_like(tw), w13, s13, w2, s2, want_f64=True)
+    assert np.all(z == 0.0)
