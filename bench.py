@@ -504,6 +504,61 @@ def producer_table(fb, torch, dev, stream, peak: float):
     return out
 
 
+MOE_E, MOE_H, MOE_S = 513, 4096, 11
+MOE_CONFIGS = [("TP4", 256, [1, 4, 8, 16, 20]), ("TP8", 128, [1, 16, 48])]
+
+
+def moe_table(fb, torch, dev, stream, peak: float):
+    """The small-M FP8 block-scale MoE layer at Qwen3.5-397B sizes (513 experts,
+    11 slots per token, hidden 4096; intermediate 256 at TP4, 128 at TP8).
+    Weights: one layer, 1.6 GB (TP4) / 0.8 GB (TP8), larger than L2.  Each
+    graph holds 24 calls with 24 different routings, so the active experts
+    change from call to call.  Algorithmic bytes of a call: the w13 / w2 bytes
+    and block scales of its distinct active experts, plus x, y, ids and
+    weights."""
+    import synth
+    out = {"E": MOE_E, "H": MOE_H, "S": MOE_S, "configs": {}}
+    for name, I, ms in MOE_CONFIGS:
+        w = synth.w_f32_torch(MOE_E * 2 * I, MOE_H, seed=950, device=dev)
+        w13, s13 = fb.fp8bs_quant_weight(w, fb.FP8BS_SCALE_F32)
+        del w
+        w = synth.w_f32_torch(MOE_E * MOE_H, I, seed=951, device=dev)
+        w2, s2 = fb.fp8bs_quant_weight(w, fb.FP8BS_SCALE_F32)
+        del w
+        torch.cuda.empty_cache()
+        w13 = w13.view(MOE_E, 2 * I, MOE_H)
+        s13 = s13.view(MOE_E, 2 * I // 128, MOE_H // 128)
+        w2 = w2.view(MOE_E, MOE_H, I)
+        s2 = s2.view(MOE_E, MOE_H // 128, I // 128)
+        per_expert = 3 * I * MOE_H + (3 * I * MOE_H // 16384) * 4
+        rows = {}
+        for M in ms:
+            routes = [synth.moe_routing(M, MOE_S, MOE_E, seed=960 + 31 * M + c) for c in range(COPIES)]
+            ids = [torch.from_numpy(r[0]).to(dev) for r in routes]
+            tws = [torch.from_numpy(r[1]).to(dev) for r in routes]
+            x = synth.x_bf16_torch(M, MOE_H, seed=970 + M, device=dev)
+            y = torch.empty((M, MOE_H), dtype=torch.bfloat16, device=dev)
+            ws = fb.new_moe_workspace(M, MOE_S, MOE_H, I, dev)
+            us = graph_us_per_call(torch, stream, lambda i: fb.fp8bs_moe_w8a16(
+                x, ids[i], tws[i], w13, s13, w2, s2, y=y, workspace=ws), COPIES, 20)
+            rc = fb.fp8bs_check_error(ws, stream)
+            if rc != 0:
+                raise SystemExit(f"MoE {name} M={M}: device error {fb.fp8bs_status_string(rc)}")
+            active = statistics.mean(len(set(r[0].ravel().tolist())) for r in routes)
+            nbytes = active * per_expert + 4 * M * MOE_H + 8 * M * MOE_S
+            gbps = nbytes / us / 1e3
+            rows[str(M)] = {"us": round(us, 2), "active_experts": round(active, 1),
+                            "bytes": int(nbytes), "GBps": round(gbps, 1), "frac": round(gbps / peak, 3)}
+            del ids, tws, x, y, ws
+        out["configs"][f"{name} I={I}"] = rows
+        del w13, s13, w2, s2
+        torch.cuda.empty_cache()
+    out["peak"] = peak
+    out["kernels"] = "moe_gate_up_kernel, moe_down_kernel, moe_combine_kernel"
+    out["bound"] = "hbm"
+    return out
+
+
 def hbm_peak():
     """(GB/s, source): the measured copy bandwidth, else the fallback figure."""
     try:
@@ -531,6 +586,10 @@ def run_gpu(args):
     fb.build()
     fb.lib()
     stream = torch.cuda.Stream(device=dev)
+    if args.moe_only:
+        if rank == 0:
+            print(json.dumps({"moe_w8a16": moe_table(fb, torch, dev, stream, hbm_peak()[0])}), flush=True)
+        return 0
     if args.producer_only:
         if rank == 0:
             line = {"producer_rmsnorm_quant": producer_table(fb, torch, dev, stream, hbm_peak()[0])}
@@ -584,6 +643,10 @@ def run_gpu(args):
     if rank == 0 and not args.no_producer:
         progress("RMSNorm + quant producer")
         producer = producer_table(fb, torch, dev, stream, peak)
+    moe = None
+    if rank == 0 and not args.no_moe:
+        progress("MoE layer")
+        moe = moe_table(fb, torch, dev, stream, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -604,6 +667,7 @@ def run_gpu(args):
             "per_m_two_launch_us_and_GBps": per_m_two,
             "m_above_32_us_and_GBps": above_32,
             "producer_rmsnorm_quant": producer,
+            "moe_w8a16": moe,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": dram_traffic_per_launch(args.workload),
                          "peak_source": peak_src, "kernel": "fused_quant_gemm_kernel",
@@ -637,6 +701,9 @@ def main(argv=None):
                     help="skip the RMSNorm + quant producer's table")
     ap.add_argument("--producer-only", action="store_true",
                     help="time only the RMSNorm + quant producer and print its table")
+    ap.add_argument("--no-moe", action="store_true", help="skip the MoE layer's table")
+    ap.add_argument("--moe-only", action="store_true",
+                    help="time only the MoE layer and print its table")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain launches instead of programmatic dependent launch")
     ap.add_argument("--no-graph", action="store_true",

@@ -34,6 +34,7 @@ STATUS = {
     -4: "FP8BS_ERR_SCALE_KIND", -5: "FP8BS_ERR_WORKSPACE", -6: "FP8BS_ERR_CUDA",
     -7: "FP8BS_ERR_TIMEOUT", -8: "FP8BS_ERR_DEVICE",
 }
+globals().update({name: code for code, name in STATUS.items()})
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfp8bs.so")
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
             "fp8bs_encode_e4m3": ([vp, i64, vp, vp], ci),
             "fp8bs_quant": ([vp, i64, i64, i64, ci, vp, vp, vp], ci),
             "fp8bs_rmsnorm_quant": ([vp, i64, i64, i64, vp, ctypes.c_float, ci, vp, vp, vp, i64, vp], ci),
+            "fp8bs_moe_workspace_bytes": ([i64, i64, i64, i64], ctypes.c_size_t),
+            "fp8bs_moe_w8a16": ([vp, i64, i64, vp, vp, i64, vp, vp, vp, vp, i64, i64, vp, vp,
+                                 ctypes.c_size_t, vp], ci),
             "fp8bs_quant_weight": ([vp, i64, i64, i64, ci, vp, vp, vp], ci),
             "fp8bs_packed_weight_bytes": ([i64, i64, ci], sz),
             "fp8bs_prepack_weight": ([vp, i64, vp, i64, i64, ci, vp, sz, vp], ci),
@@ -197,6 +201,49 @@ def fp8bs_rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
                                    y.stride(0) if y is not None else 0, _stream(stream))
     _check(rc, "fp8bs_rmsnorm_quant")
     return xq, xs, y
+
+
+def fp8bs_moe_workspace_bytes(M: int, S: int, H: int, I: int) -> int:
+    return int(lib().fp8bs_moe_workspace_bytes(int(M), int(S), int(H), int(I)))
+
+
+def new_moe_workspace(M: int, S: int, H: int, I: int, device=None) -> torch.Tensor:
+    """Allocate (with torch) a zeroed MoE workspace for up to M tokens x S slots."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    n = fp8bs_moe_workspace_bytes(M, S, H, I)
+    if n == 0:
+        raise Fp8bsError(FP8BS_ERR_SHAPE, "fp8bs_moe_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def fp8bs_moe_w8a16(x: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor,
+                    w13: torch.Tensor, s13: torch.Tensor, w2: torch.Tensor, s2: torch.Tensor,
+                    y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """One small-M MoE layer: bf16 x [M, H]; int32 topk_ids and fp32 topk_w
+    [M, S]; e4m3 (uint8) w13 [E, 2I, H] with fp32 s13 [E, 2I/128, H/128]; w2
+    [E, H, I] with s2 [E, H/128, I/128].  Returns bf16 y [M, H]."""
+    _require_cuda(x, topk_ids, topk_w, w13, s13, w2, s2, y, workspace)
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    assert topk_ids.dtype == torch.int32 and topk_w.dtype == torch.float32
+    assert topk_ids.is_contiguous() and topk_w.is_contiguous() and topk_ids.shape == topk_w.shape
+    for t in (w13, s13, w2, s2):
+        assert t.is_contiguous()
+    assert w13.dtype == torch.uint8 and w2.dtype == torch.uint8
+    assert s13.dtype == torch.float32 and s2.dtype == torch.float32
+    M, H = x.shape
+    S = topk_ids.shape[1]
+    E, I2, _ = w13.shape
+    I = I2 // 2
+    if y is None:
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = new_moe_workspace(M, S, H, I, x.device)
+    rc = lib().fp8bs_moe_w8a16(_ptr(x), M, H, _ptr(topk_ids), _ptr(topk_w), S, _ptr(w13), _ptr(s13),
+                               _ptr(w2), _ptr(s2), E, I, _ptr(y), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    _check(rc, "fp8bs_moe_w8a16")
+    return y
 
 
 def fp8bs_quant_weight(w: torch.Tensor, scale_kind: int = FP8BS_SCALE_F32, stream=None):

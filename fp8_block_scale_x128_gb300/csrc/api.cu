@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "internal.cuh"
+#include "moe.cuh"
 #include "producer.cuh"
 
 namespace {
@@ -139,6 +140,45 @@ int fp8bs_rmsnorm_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, co
         (scale_kind == FP8BS_SCALE_F32 && !aligned(xs, 4)) || (y && (!aligned(y, 16) || ldy % 8 != 0)))
         return FP8BS_ERR_ALIGN;
     return status_of(launch_rmsnorm_quant(x, M, K, ldx, gamma, eps, scale_kind, xq, xs, y, ldy, as_stream(stream)));
+}
+size_t fp8bs_moe_workspace_bytes(int64_t M, int64_t S, int64_t H, int64_t I) {
+    if (M < 0 || S < 1 || M * S > FP8BS_MOE_MAX_PAIRS || H < 512 || H % 512 != 0 || H > kMaxDim ||
+        (I != 128 && I != 256 && I != FP8BS_MOE_MAX_I))
+        return 0;
+    return moe_workspace_bytes(M, S, H, I);
+}
+int fp8bs_moe_w8a16(const uint16_t* x, int64_t M, int64_t H, const int32_t* topk_ids, const float* topk_w,
+                    int64_t S, const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2, int64_t E,
+                    int64_t I, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || S < 1 || M * S > FP8BS_MOE_MAX_PAIRS || E < 1 || E > FP8BS_MOE_MAX_EXPERTS || H < 512 ||
+        H % 512 != 0 || H > kMaxDim || (I != 128 && I != 256 && I != FP8BS_MOE_MAX_I))
+        return FP8BS_ERR_SHAPE;
+    if (M == 0) return FP8BS_OK;
+    if (!x || !topk_ids || !topk_w || !w13 || !s13 || !w2 || !s2 || !y || !workspace) return FP8BS_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(w13, 16) || !aligned(s13, 4) ||
+        !aligned(w2, 16) || !aligned(s2, 4) || !aligned(y, 8) || !aligned(workspace, 256))
+        return FP8BS_ERR_ALIGN;
+    if (workspace_bytes < moe_workspace_bytes(M, S, H, I)) return FP8BS_ERR_WORKSPACE;
+    int sm = 0;
+    const int rc = current_sm_count(&sm);
+    if (rc != FP8BS_OK) return rc;
+    MoeArgs a;
+    a.x = x;
+    a.ids = topk_ids;
+    a.tw = topk_w;
+    a.w13 = w13;
+    a.s13 = s13;
+    a.w2 = w2;
+    a.s2 = s2;
+    a.y = y;
+    a.workspace = static_cast<uint8_t*>(workspace);
+    a.M = static_cast<int>(M);
+    a.S = static_cast<int>(S);
+    a.H = static_cast<int>(H);
+    a.I = static_cast<int>(I);
+    a.E = static_cast<int>(E);
+    a.sm_count = sm;
+    return status_of(launch_moe(a, as_stream(stream)));
 }
 int fp8bs_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int scale_kind, uint8_t* wq,
                        void* ws, void* stream) {

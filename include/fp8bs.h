@@ -263,6 +263,58 @@ int fp8bs_gemm_prequant(const uint8_t* xq, int64_t M, int64_t ldxq, const void* 
  * fp8bs_workspace_init before the workspace is used again. */
 int fp8bs_check_error(void* workspace, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Small-M FP8 block-scale MoE layer ([P2] "Modifications")                  */
+/* ------------------------------------------------------------------------ */
+
+#define FP8BS_MOE_MAX_PAIRS 1024    /* M * S: routed (token, slot) pairs    */
+#define FP8BS_MOE_MAX_EXPERTS 4096  /* E                                     */
+#define FP8BS_MOE_MAX_I 512         /* intermediate size per expert          */
+
+/* Workspace bytes of fp8bs_moe_w8a16: a 256-byte error word, the gate/up
+ * partial sums (M*S x H/512 x 2I fp32) and the per-slot down projections
+ * (M*S x H fp32).  Returns 0 for an unsupported shape. */
+size_t fp8bs_moe_workspace_bytes(int64_t M, int64_t S, int64_t H, int64_t I);
+
+/* One MoE layer at decode sizes, the FP8 small-M kernel of [P2]
+ * "Modifications": float8_e4m3fn w13 / w2 with contiguous 128x128 fp32 block
+ * scales, each block's scale applied to its partial sum, bf16 activations,
+ * routing given per token (no sort).  Per token m and slot s, with
+ * e = topk_ids[m, s]:
+ *   h    = x[m] . w13[e]^T   (w13[e] stacks the gate rows 0..I-1 over the up
+ *                             rows I..2I-1; per 128-wide K block the partial
+ *                             sum times its scale, fp32)
+ *   a    = bf16(silu(h_gate) * h_up),  silu(g) = g / (1 + exp(-g))
+ *   o    = a . w2[e]^T        (same block-scale rule)
+ *   y[m] = bf16(sum over s, in slot order, of topk_w[m, s] * o)
+ *   x        : bf16 [M, H], 16-byte aligned, rows contiguous; finite values
+ *              below 2^64 in magnitude (the weights are decoded as exact
+ *              power-of-two-scaled values, and x carries the 2^64).
+ *   M, S     : tokens and slots per token, M >= 0 (0 is a no-op), S >= 1,
+ *              M * S <= FP8BS_MOE_MAX_PAIRS.
+ *   H        : hidden size, a multiple of 512.
+ *   topk_ids : int32 [M, S] expert ids; an id outside [0, E) makes that slot
+ *              contribute nothing and records FP8BS_ERR_DEVICE in the
+ *              workspace error word.
+ *   topk_w   : fp32 [M, S] routing weights.
+ *   w13, s13 : e4m3fn [E, 2I, H] (16-byte aligned), fp32 [E, 2I/128, H/128].
+ *   w2, s2   : e4m3fn [E, H, I] (16-byte aligned), fp32 [E, H/128, I/128].
+ *   E, I     : experts (1..FP8BS_MOE_MAX_EXPERTS); I in {128, 256, 512}.
+ *   y        : bf16 [M, H], 8-byte aligned.
+ *   workspace: fp8bs_moe_workspace_bytes(M, S, H, I) bytes, 256-byte aligned;
+ *              its first word must be zero before the first call (e.g.
+ *              fp8bs_workspace_init); fp8bs_check_error reads it.
+ * Three launches on `stream` (gate/up, down, combine), the last two with
+ * programmatic dependent launch; no cross-CTA waits; every sum in a fixed
+ * order, so results are deterministic.  Each active expert's weights are read
+ * once per call, whatever number of tokens it serves.
+ * Errors: FP8BS_ERR_SHAPE, FP8BS_ERR_ARG, FP8BS_ERR_ALIGN,
+ * FP8BS_ERR_WORKSPACE, FP8BS_ERR_CUDA. */
+int fp8bs_moe_w8a16(const uint16_t* x, int64_t M, int64_t H, const int32_t* topk_ids,
+                    const float* topk_w, int64_t S, const uint8_t* w13, const float* s13,
+                    const uint8_t* w2, const float* s2, int64_t E, int64_t I, uint16_t* y,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Limits of fp8bs_gemm_fused_static's fixed scratch. */
 #define FP8BS_STATIC_MAX_K 16384  /* largest K it accepts                   */
 #define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */

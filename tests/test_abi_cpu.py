@@ -196,6 +196,35 @@ def test_rmsnorm_quant_host_checks(L):
     assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P, P, 4100, STREAM) == ALIGN
 
 
+def test_moe_host_checks(L):
+    wsb = L.fp8bs_moe_workspace_bytes
+    # 256-byte error word + gate/up partials (M*S x H/512 x 2I) + down outputs (M*S x H), fp32
+    assert wsb(16, 11, 4096, 256) == 256 + 16 * 11 * 8 * 512 * 4 + 16 * 11 * 4096 * 4
+    assert wsb(16, 11, 4000, 256) == 0
+    assert wsb(16, 11, 4096, 384) == 0
+    assert wsb(100, 11, 4096, 256) == 0  # more than 1024 pairs
+    n = wsb(4, 11, 4096, 256)
+    m = L.fp8bs_moe_w8a16
+    # x, M, H, ids, w, S, w13, s13, w2, s2, E, I, y, ws, ws_bytes, stream
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 513, 256, P, P, n - 1, STREAM) == WS
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 513, 200, P, P, n, STREAM) == SHAPE
+    assert m(P, 4, 4100, P, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == SHAPE
+    assert m(P, 4, 4096, P, P, 0, P, P, P, P, 513, 256, P, P, n, STREAM) == SHAPE
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 0, 256, P, P, n, STREAM) == SHAPE
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 5000, 256, P, P, n, STREAM) == SHAPE
+    assert m(P, 100, 4096, P, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == SHAPE
+    assert m(P, -1, 4096, P, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == SHAPE
+    assert m(None, 0, 4096, None, None, 11, None, None, None, None, 513, 256, None, None, 0, STREAM) == OK
+    assert m(P, 4, 4096, None, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == ARG
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 513, 256, None, P, n, STREAM) == ARG
+    assert m(P + 8, 4, 4096, P, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == ALIGN
+    assert m(P, 4, 4096, P + 2, P, 11, P, P, P, P, 513, 256, P, P, n, STREAM) == ALIGN
+    assert m(P, 4, 4096, P, P, 11, P + 8, P, P, P, 513, 256, P, P, n, STREAM) == ALIGN
+    assert m(P, 4, 4096, P, P, 11, P, P, P + 4, P, 513, 256, P, P, n, STREAM) == ALIGN
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 513, 256, P + 4, P, n, STREAM) == ALIGN
+    assert m(P, 4, 4096, P, P, 11, P, P, P, P, 513, 256, P, P + 128, n, STREAM) == ALIGN
+
+
 def test_prepack_and_weight_quant_host_checks(L):
     pp = L.fp8bs_prepack_weight
     assert pp(P, 4096, P, 5120, 4096, 5, P, 1 << 30, STREAM) == ARG
