@@ -132,28 +132,48 @@ __device__ void build_list(const MoeParams& p, Route& rs, int e) {
     __syncthreads();
 }
 
-// 16 e4m3fn codes -> 16 fp32 values, each exactly 2^-120 times the code's
-// value, with integer operations only (no conversion instruction, whose
-// throughput bounds a decode-heavy loop).  The code's 7 magnitude bits become
-// fp32 bits 20-26 (exponent field = the e4m3 exponent, mantissa top = its 3
-// bits) and its sign bit 31: a normal code 2^(e-7)(1 + m/8) lands on
-// 2^(e-127)(1 + m/8) and a subnormal m 2^-9 on the fp32 subnormal m 2^-129.
-// Callers give the other factor 2^64 (kXScale) and the partial sums 2^56
-// (kAccScale), so products stay normal fp32 numbers and every scaling is an
-// exact power of two.
+// Weight decode with integer operations only (no conversion instruction): a
+// code's 7 magnitude bits become bits 4-10 of a bf16 (exponent field = the
+// e4m3 exponent, mantissa top = its 3 bits) and its sign bit 15, so a normal
+// code 2^(e-7)(1 + m/8) lands on 2^(e-127)(1 + m/8) and a subnormal m 2^-9 on
+// the bf16 subnormal m 2^-129: exactly 2^-120 times the code's value.  The
+// other factor carries 2^64 (kXScale) and the partial sums 2^56 (kAccScale),
+// so every product is a normal fp32 number and every scaling an exact power of
+// two.  Products and sums use the mixed-precision FMA (bf16 inputs, fp32
+// accumulate): each product is exact.
 constexpr float kXScale = 0x1p64f;
 constexpr float kAccScale = 0x1p56f;
 
-__device__ __forceinline__ void decode16(const uint4& w, float (&f)[16]) {
-    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t v = words[q];
-        f[4 * q + 0] = __uint_as_float(((v << 20) & 0x07F00000u) | ((v << 24) & 0x80000000u));
-        f[4 * q + 1] = __uint_as_float(((v << 12) & 0x07F00000u) | ((v << 16) & 0x80000000u));
-        f[4 * q + 2] = __uint_as_float(((v << 4) & 0x07F00000u) | ((v << 8) & 0x80000000u));
-        f[4 * q + 3] = __uint_as_float(((v >> 4) & 0x07F00000u) | (v & 0x80000000u));
-    }
+// One weight word (4 codes) -> two bf16 pairs, each value exactly 2^-120
+// times the code's value (the bf16 form of the decode above): even holds
+// codes 0 and 2, odd codes 1 and 3.
+__device__ __forceinline__ void decode4_bf16(uint32_t v, uint32_t& even, uint32_t& odd) {
+    even = ((v << 4) & 0x07F007F0u) | ((v << 8) & 0x80008000u);
+    odd = ((v >> 4) & 0x07F007F0u) | (v & 0x80008000u);
+}
+
+// acc + a.lo * b.lo + a.hi * b.hi: bf16 inputs, fp32 products (exact) and sums.
+__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float acc) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
+// Two bf16 words (values 0,1 and 2,3) scaled by 2^64, regrouped as the weight
+// decode pairs them: even = (0, 2), odd = (1, 3).  Exact (a power-of-two
+// scaling of bf16 values below 2^64).
+__device__ __forceinline__ void scale_pair_bf16(uint32_t w01, uint32_t w23, uint32_t& even, uint32_t& odd) {
+    uint32_t s01, s23;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(s01)
+        : "f"(__uint_as_float(w01 & 0xFFFF0000u) * kXScale), "f"(__uint_as_float(w01 << 16) * kXScale));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(s23)
+        : "f"(__uint_as_float(w23 & 0xFFFF0000u) * kXScale), "f"(__uint_as_float(w23 << 16) * kXScale));
+    even = __byte_perm(s01, s23, 0x5410);
+    odd = __byte_perm(s01, s23, 0x7632);
 }
 
 __device__ __forceinline__ float bf16_round(float v) {
@@ -172,32 +192,35 @@ __device__ __forceinline__ float bf16_round(float v) {
 template <int NP>
 __device__ __forceinline__ void gate_up_rows(const MoeParams& p, const Route& rs, const uint8_t* sW, int pb, int ks,
                                              int KS, int I2, int row0, float scale, int lane) {
-    float xf[NP][16];
+    uint32_t xe[NP][4], xo[NP][4];  // this lane's 16 x values, scaled and paired as the decode pairs
 #pragma unroll
     for (int t = 0; t < NP; ++t) {
         const int m = rs.list[pb + t] / p.S;
         const uint4* src =
             reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(m) * p.H + ks * kSplitCols + lane * 16);
-        float v[8];
-        unpack_bf16x8(src[0], v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xf[t][j] = v[j] * kXScale;
-        unpack_bf16x8(src[1], v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xf[t][8 + j] = v[j] * kXScale;
+        const uint4 lo = src[0], hi = src[1];
+        scale_pair_bf16(lo.x, lo.y, xe[t][0], xo[t][0]);
+        scale_pair_bf16(lo.z, lo.w, xe[t][1], xo[t][1]);
+        scale_pair_bf16(hi.x, hi.y, xe[t][2], xo[t][2]);
+        scale_pair_bf16(hi.z, hi.w, xe[t][3], xo[t][3]);
     }
     ptx::cp_async_wait_all();
     __syncwarp();
 #pragma unroll 4
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const uint4 wv = *reinterpret_cast<const uint4*>(sW + r * kSplitCols + lane * 16);
-        float wf[16];
-        decode16(wv, wf);
+        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t we[4], wo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) decode4_bf16(words[q], we[q], wo[q]);
 #pragma unroll
         for (int t = 0; t < NP; ++t) {
             float acc = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc = fmaf(xf[t][j], wf[j], acc);
+            for (int q = 0; q < 4; ++q) {
+                acc = fma2_bf16(xe[t][q], we[q], acc);
+                acc = fma2_bf16(xo[t][q], wo[q], acc);
+            }
             acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
             acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
             acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
@@ -249,13 +272,13 @@ __global__ void __launch_bounds__(kMoeThreads) moe_gate_up_kernel(const __grid_c
 // each, 8 lanes per 128-column block), 32 / (I/16) rows per warp step.
 __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const __grid_constant__ MoeParams p) {
     __shared__ Route rs;
-    extern __shared__ __align__(16) uint8_t smem2[];  // weights [8 warps][8 rows][I], then a [kDownBatch][I]
+    extern __shared__ __align__(16) uint8_t smem2[];  // weights [8 warps][8 rows][I], then a [kDownBatch][I] bf16
     route_setup(p, rs);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int I = p.I, I2 = 2 * I, NT = p.H / kItemRows, KS = p.H / kSplitCols, IB = I / kTile;
     const int items = rs.n_active * NT;
     uint8_t* sW = smem2 + warp * kRowsPerWarp * I;
-    float* sA = reinterpret_cast<float*>(smem2 + kItemRows * I);
+    uint16_t* sA = reinterpret_cast<uint16_t*>(smem2 + kItemRows * I);
     // the first item's weights do not depend on the previous launch
     if (tid == 0 && static_cast<int>(blockIdx.x) < items) {
         const int e = rs.active[blockIdx.x / NT], nt = blockIdx.x % NT;
@@ -289,29 +312,39 @@ __global__ void __launch_bounds__(kMoeThreads) moe_down_kernel(const __grid_cons
                     g += P[ks * I2 + i];
                     u += P[ks * I2 + I + i];
                 }
-                // interleaved: float4 j of lane chunk c at (j * cpr + c), so the
-                // lanes of a row read consecutive 16-byte words
-                const int c = i >> 4, j = (i >> 2) & 3;
-                sA[t * I + (j * cpr + c) * 4 + (i & 3)] = bf16_round(g / (1.0f + expf(-g)) * u) * kXScale;
+                // a * 2^64 as bf16 (exact), laid out as the weight decode pairs the
+                // values: for lane chunk c (values 16c .. 16c+15), word q of the
+                // even half holds values 4q and 4q+2, of the odd half 4q+1 and
+                // 4q+3; the two 16-byte halves of chunk c sit at uint4 index
+                // (h * cpr + c), so the lanes of a row read consecutive words
+                const float v = bf16_round(g / (1.0f + expf(-g)) * u) * kXScale;
+                uint16_t bits;
+                asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(bits) : "f"(v));
+                const int c = i >> 4, k = i & 15, q = k >> 2, h = k & 1, half = (k >> 1) & 1;
+                sA[t * I + ((h * cpr + c) * 4 + q) * 2 + half] = bits;
             }
             ptx::cp_async_wait_all();
             __syncthreads();
             for (int r0 = 0; r0 < kRowsPerWarp; r0 += rpw) {
                 const int row = row_base + r0 + lr;
                 const uint4 wv = *reinterpret_cast<const uint4*>(sW + (r0 + lr) * I + lc * 16);
-                float wf[16];
-                decode16(wv, wf);
+                uint32_t we[4], wo[4];
+                decode4_bf16(wv.x, we[0], wo[0]);
+                decode4_bf16(wv.y, we[1], wo[1]);
+                decode4_bf16(wv.z, we[2], wo[2]);
+                decode4_bf16(wv.w, we[3], wo[3]);
                 for (int t = 0; t < np; ++t) {
-                    const float4* av = reinterpret_cast<const float4*>(sA + t * I) + lc;
+                    const uint4* av = reinterpret_cast<const uint4*>(sA + t * I) + lc;
+                    const uint4 ae = av[0], ao = av[cpr];
                     float acc = 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float4 q = av[j * cpr];
-                        acc = fmaf(q.x, wf[4 * j], acc);
-                        acc = fmaf(q.y, wf[4 * j + 1], acc);
-                        acc = fmaf(q.z, wf[4 * j + 2], acc);
-                        acc = fmaf(q.w, wf[4 * j + 3], acc);
-                    }
+                    acc = fma2_bf16(ae.x, we[0], acc);
+                    acc = fma2_bf16(ao.x, wo[0], acc);
+                    acc = fma2_bf16(ae.y, we[1], acc);
+                    acc = fma2_bf16(ao.y, wo[1], acc);
+                    acc = fma2_bf16(ae.z, we[2], acc);
+                    acc = fma2_bf16(ao.z, wo[2], acc);
+                    acc = fma2_bf16(ae.w, we[3], acc);
+                    acc = fma2_bf16(ao.w, wo[3], acc);
                     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
                     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
                     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
@@ -405,7 +438,7 @@ cudaError_t launch_moe(const MoeArgs& a, cudaStream_t stream) {
     static int occ1[64] = {0};
     static int occ2[64][3] = {{0}};
     const size_t smem1 = static_cast<size_t>(kItemRows) * kSplitCols;
-    const size_t smem2 = static_cast<size_t>(kItemRows) * a.I + static_cast<size_t>(kDownBatch) * a.I * sizeof(float);
+    const size_t smem2 = static_cast<size_t>(kItemRows) * a.I + static_cast<size_t>(kDownBatch) * a.I * sizeof(uint16_t);
     const int ii = a.I == 128 ? 0 : (a.I == 256 ? 1 : 2);
     cudaError_t e;
     if (occ1[dev] == 0) {
@@ -414,7 +447,7 @@ cudaError_t launch_moe(const MoeArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kItemRows * FP8BS_MOE_MAX_I +
-                                                  kDownBatch * FP8BS_MOE_MAX_I * sizeof(float)));
+                                                  kDownBatch * FP8BS_MOE_MAX_I * sizeof(uint16_t)));
         if (e != cudaSuccess) return e;
         int n = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe_gate_up_kernel, kMoeThreads, smem1);
