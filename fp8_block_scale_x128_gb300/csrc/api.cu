@@ -55,6 +55,34 @@ int current_sm_count(int* out) {
 
 size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_count, K); }
 
+// From this many tokens the fused call runs the quant and the GEMM on its
+// codes as two launches, measured faster there than the 64-token fused kernel
+// (whose in-kernel exchange grows with M); [P1] "Motivation" likewise keeps
+// larger inputs on the library path.
+constexpr int kTwoLaunchMinM = 40;
+
+// The fused call, routed: below kTwoLaunchMinM one launch; from it on the
+// 1x128 quant, then the GEMM on those codes.  The codes and scales go to
+// xq_out / xs_out when the caller asked for them, else to the workspace's
+// activation records, which the GEMM on given codes does not use (room for
+// 64 rows of codes and fp32 scales per K block).
+cudaError_t launch_fused_routed(FusedArgs a, cudaStream_t stream) {
+    if (a.M < kTwoLaunchMinM) return launch_fused(a, stream);
+    uint8_t* act = a.workspace + ws_act_offset(a.sm_count);
+    uint8_t* xq = a.xq_out ? a.xq_out : act;
+    void* xs = a.xs_out ? a.xs_out : static_cast<void*>(act + static_cast<size_t>(a.M) * a.K);
+    const cudaError_t e = launch_quant(a.x, a.M, a.K, a.ldx, a.kind, xq, xs, stream);
+    if (e != cudaSuccess) return e;
+    a.xq_in = xq;
+    a.ldxq = a.K;
+    a.xs_in = xs;
+    a.xq_out = nullptr;
+    a.xs_out = nullptr;
+    return launch_fused(a, stream);
+}
+static_assert(static_cast<size_t>(FP8BS_MAX_M) * (kTile + sizeof(float)) <= kKbRecBytes,
+              "the activation records hold a routed call's codes and scales");
+
 // Scratch of fp8bs_gemm_fused_static: one fixed array per device, laid out like
 // a caller's workspace for FP8BS_STATIC_MAX_SMS CTAs and K up to
 // FP8BS_STATIC_MAX_K.
@@ -260,7 +288,7 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     a.sm_count = sm;
     a.timeout_cycles = kDefaultTimeoutCycles;
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
-    return status_of(launch_fused(a, as_stream(stream)));
+    return status_of(launch_fused_routed(a, as_stream(stream)));
 }
 
 int fp8bs_gemm_prequant(const uint8_t* xq, int64_t M, int64_t ldxq, const void* xs, const void* packed,
@@ -342,7 +370,7 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
     a.sm_count = sm;
     a.timeout_cycles = kDefaultTimeoutCycles;
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
-    rc = status_of(launch_fused(a, as_stream(stream)));
+    rc = status_of(launch_fused_routed(a, as_stream(stream)));
     if (rc != FP8BS_OK || !status_out) return rc;
     return status_of(cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
                                      as_stream(stream)));

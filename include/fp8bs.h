@@ -229,6 +229,11 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *   flags    : 0 or FP8BS_FLAG_PDL.
  * The result is deterministic: the split-K partials are summed in a fixed
  * order, so repeated calls and graph replays give identical bits.
+ * Up to 39 tokens the call is one launch.  From 40 tokens on it is two: the
+ * 1x128 quant (into xq_out / xs_out when given, else into the workspace),
+ * then the GEMM on those codes, the same kernels as fp8bs_quant followed by
+ * fp8bs_gemm_prequant and bit-identical to them; that pair was measured
+ * faster there than the 64-token single launch.
  * The CTAs of one launch exchange data, so a call assumes the whole device:
  * one CTA per multiprocessor, all resident together.  (Under a partition of
  * the GPU with fewer multiprocessors the bounded waits expire and the call
