@@ -37,10 +37,29 @@ def digests(name, M, N, K, kind, seed):
     return out
 
 
+# RMSNorm producer cases (square root and division only: IEEE-exact on every
+# machine).  name, M, K, kind, seed
+RMS_CASES = [
+    ("rms_f32_m3_k640", 3, 640, 0, 21),
+    ("rms_ue8m0_m4_k1024", 4, 1024, 1, 22),
+]
+
+
+def rms_digests(name, M, K, kind, seed):
+    x = synth.x_bf16(M, K, seed=seed)
+    g = synth.gamma_bf16(K, seed=seed + 500)
+    y, xq, xs = oracle.rmsnorm_quant(x, g, 1e-6, kind)
+    return {label: hashlib.sha256(arr.tobytes()).hexdigest()[:32]
+            for label, arr in (("x", x), ("gamma", g), ("y", y), ("xq", xq), ("xs", xs))}
+
+
 def main():
     lines = ["# case label sha256[:32] -- written by make_golden.py from the oracle only"]
     for case in CASES:
         for label, h in digests(*case).items():
+            lines.append(f"{case[0]} {label} {h}")
+    for case in RMS_CASES:
+        for label, h in rms_digests(*case).items():
             lines.append(f"{case[0]} {label} {h}")
     with open(os.path.join(HERE, "oracle_digests.txt"), "w") as f:
         f.write("\n".join(lines) + "\n")

@@ -196,6 +196,16 @@ def test_rmsnorm_quant_host_checks(L):
     assert r(P, 2, 4096, 4096, P, 1e-6, 0, P, P, P, 4100, STREAM) == ALIGN
 
 
+def test_header_states_the_fixed_scratch_size(L):
+    # the fixed scratch of fp8bs_gemm_fused_static is a workspace laid out for
+    # FP8BS_STATIC_MAX_SMS CTAs and K = FP8BS_STATIC_MAX_K; the header states its size
+    import re
+    text = open(fb.HEADER_PATH).read()
+    stated = int(re.search(r"fixed device array inside this library \(([0-9,]+) bytes", text).group(1)
+                 .replace(",", ""))
+    assert L.fp8bs_workspace_bytes(128, fb.FP8BS_STATIC_MAX_K, fb.FP8BS_STATIC_MAX_SMS) == stated
+
+
 def test_moe_host_checks(L):
     wsb = L.fp8bs_moe_workspace_bytes
     # 256-byte error word + gate/up partials (M*S x H/512 x 2I) + down outputs (M*S x H), fp32

@@ -23,3 +23,8 @@ def _stored():
 @pytest.mark.parametrize("case", make_golden.CASES, ids=[c[0] for c in make_golden.CASES])
 def test_oracle_digests_are_stable(oracle_mod, case):
     assert make_golden.digests(*case) == _stored()[case[0]]
+
+
+@pytest.mark.parametrize("case", make_golden.RMS_CASES, ids=[c[0] for c in make_golden.RMS_CASES])
+def test_oracle_rmsnorm_digests_are_stable(oracle_mod, case):
+    assert make_golden.rms_digests(*case) == _stored()[case[0]]
