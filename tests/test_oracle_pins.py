@@ -598,3 +598,16 @@ def test_moe_is_linear_in_the_routing_weights(oracle_mod):
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
     _, z = oracle_mod.moe_w8a16(x, ids, np.zeros_like(tw), w13, s13, w2, s2, want_f64=True)
     assert np.all(z == 0.0)
+
+
+def test_integer_e4m3_decode_identity_used_by_the_moe_kernels(oracle_mod):
+    # the MoE kernels decode a code c with integer operations only: its 7
+    # magnitude bits to bf16 bits 4-10 and its sign to bit 15, which is the
+    # code's value times 2^-120 for every finite code, subnormals included
+    # (checked here exactly, against the oracle's decode from the format)
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue  # NaN codes
+        bits = ((c & 0x7F) << 4) | ((c & 0x80) << 8)
+        v = float(synth.bf16_bits_to_f32(np.array([bits], np.uint16))[0])
+        assert math.ldexp(v, 120) == oracle_mod.e4m3_decode(c), hex(c)
