@@ -61,3 +61,23 @@ def test_bench_rejects_short_warmup():
     import bench
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    # one bounded oracle step of the M sweep: the line carries every key of the
+    # benchmark contract, with the reference arm's own e2e and cpu_baseline
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"].startswith("M sweep")
