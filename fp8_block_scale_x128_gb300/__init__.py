@@ -56,6 +56,19 @@ def build(force: bool = False) -> str:
     return _b.build(force=force)
 
 
+def use_trace_library() -> str:
+    """Build the traced variant of the library (the fused kernel stamps its
+    phase boundaries, read back with fp8bs_trace_read) and make lib() load it.
+    Must be called before the first lib() call of the process."""
+    global LIB_PATH
+    from . import native_build as _b
+    with _lock:
+        if _lib is not None:
+            raise RuntimeError("the library is already loaded")
+        LIB_PATH = _b.build(trace=True)
+    return LIB_PATH
+
+
 def declared_functions() -> list[str]:
     """Names of the functions include/fp8bs.h declares."""
     with open(HEADER_PATH) as f:
@@ -97,6 +110,7 @@ def lib() -> ctypes.CDLL:
                                     ci),
             "fp8bs_gemm_fused_static": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, vp, vp,
                                          c.c_uint, vp], ci),
+            "fp8bs_trace_read": ([vp, sz], ci),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -375,6 +389,19 @@ def fp8bs_gemm_fused_static(x: torch.Tensor, packed: torch.Tensor, N: int, K: in
         FP8BS_FLAG_PDL if pdl else 0, _stream(stream))
     _check(rc, "fp8bs_gemm_fused_static")
     return y
+
+
+FP8BS_TRACE_CALLS, FP8BS_TRACE_CTAS, FP8BS_TRACE_POINTS = 256, 160, 48
+
+
+def fp8bs_trace_read():
+    """The traced library's timeline as a numpy uint64 array
+    [calls][CTAs][points][2] (globaltimer ns, clock64); raises in a plain build."""
+    import numpy as np
+    buf = np.zeros((FP8BS_TRACE_CALLS, FP8BS_TRACE_CTAS, FP8BS_TRACE_POINTS, 2), dtype=np.uint64)
+    rc = lib().fp8bs_trace_read(ctypes.c_void_p(buf.ctypes.data), buf.nbytes)
+    _check(rc, "fp8bs_trace_read")
+    return buf
 
 
 def fp8bs_check_error(workspace: torch.Tensor, stream=None) -> int:

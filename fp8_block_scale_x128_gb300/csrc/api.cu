@@ -12,11 +12,13 @@
 // for dense 128x128 fp8 linears (6/8)", "Modifications" requires.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.cuh"
 #include "moe.cuh"
 #include "producer.cuh"
+#include "trace.cuh"
 
 namespace {
 
@@ -37,29 +39,33 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CU
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Multiprocessor count of the current device, cached per device (relaxed
+// atomics: concurrent first calls from several host threads may both query).
 int current_sm_count(int* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
-    static int cache[64] = {0};
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-        *out = cache[dev];
-        return FP8BS_OK;
+    static std::atomic<int> cache[64];
+    if (dev >= 0 && dev < 64) {
+        const int n = cache[dev].load(std::memory_order_relaxed);
+        if (n > 0) {
+            *out = n;
+            return FP8BS_OK;
+        }
     }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return FP8BS_ERR_CUDA;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     *out = n;
     return FP8BS_OK;
 }
 
 size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_count, K); }
 
-// From this many tokens the fused call runs the quant and the GEMM on its
-// codes as two launches, measured faster there than the 64-token fused kernel
-// (whose in-kernel exchange grows with M); [P1] "Motivation" likewise keeps
-// larger inputs on the library path.
-constexpr int kTwoLaunchMinM = 40;
+// Above kFusedMaxM tokens the fused call runs the quant and the GEMM on its
+// codes as two launches: quantising every K block in every CTA grows with M,
+// and [P1] "Motivation" likewise keeps larger inputs on the library path.
+constexpr int kTwoLaunchMinM = kFusedMaxM + 1;
 
 // The fused call, routed: below kTwoLaunchMinM one launch; from it on the
 // 1x128 quant, then the GEMM on those codes.  The codes and scales go to
@@ -70,7 +76,7 @@ cudaError_t launch_fused_routed(FusedArgs a, cudaStream_t stream) {
     if (a.M < kTwoLaunchMinM) return launch_fused(a, stream);
     uint8_t* act = a.workspace + ws_act_offset(a.sm_count);
     uint8_t* xq = a.xq_out ? a.xq_out : act;
-    void* xs = a.xs_out ? a.xs_out : static_cast<void*>(act + static_cast<size_t>(a.M) * a.K);
+    void* xs = a.xs_out ? a.xs_out : static_cast<void*>(act + static_cast<size_t>(FP8BS_MAX_M) * a.K);
     const cudaError_t e = launch_quant(a.x, a.M, a.K, a.ldx, a.kind, xq, xs, stream);
     if (e != cudaSuccess) return e;
     a.xq_in = xq;
@@ -80,14 +86,12 @@ cudaError_t launch_fused_routed(FusedArgs a, cudaStream_t stream) {
     a.xs_out = nullptr;
     return launch_fused(a, stream);
 }
-static_assert(static_cast<size_t>(FP8BS_MAX_M) * (kTile + sizeof(float)) <= kKbRecBytes,
-              "the activation records hold a routed call's codes and scales");
 
 // Scratch of fp8bs_gemm_fused_static: one fixed array per device, laid out like
 // a caller's workspace for FP8BS_STATIC_MAX_SMS CTAs and K up to
 // FP8BS_STATIC_MAX_K.
 constexpr size_t kStaticScratchBytes = ws_total_bytes(FP8BS_STATIC_MAX_SMS, FP8BS_STATIC_MAX_K);
-static_assert(kStaticScratchBytes == 7426304, "fp8bs.h states the scratch size");
+static_assert(kStaticScratchBytes == 22057216, "fp8bs.h states the scratch size");
 
 __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
@@ -96,15 +100,20 @@ std::mutex g_static_mu;
 uint8_t* g_static_ptr[kStaticMaxDevices] = {};
 
 // Address of the current device's scratch; the first call per device looks it
-// up and zeroes it on `s` (the error word, the epoch words and every flag must
-// start at zero), then waits for that, so a call from another thread or stream
-// never sees a half-cleared scratch.
+// up and zeroes it on `s` (the error word and the epoch words must start at
+// zero), then waits for that, so a call from another thread or stream never
+// sees a half-cleared scratch.  That set-up synchronises `s`, which would
+// invalidate a stream capture: on a capturing stream it is refused
+// (FP8BS_ERR_ARG) before the stream is touched.
 int static_scratch(cudaStream_t s, uint8_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
     if (dev < 0 || dev >= kStaticMaxDevices) return FP8BS_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
     if (!g_static_ptr[dev]) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return FP8BS_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return FP8BS_ERR_ARG;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return FP8BS_ERR_CUDA;
         if (cudaMemsetAsync(p, 0, kStaticScratchBytes, s) != cudaSuccess) return FP8BS_ERR_CUDA;
@@ -372,8 +381,22 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     rc = status_of(launch_fused_routed(a, as_stream(stream)));
     if (rc != FP8BS_OK || !status_out) return rc;
-    return status_of(cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
-                                     as_stream(stream)));
+    // this call's status, then a clean error word for the next call (both in
+    // stream order; a memset allocates nothing)
+    if (cudaMemcpyAsync(status_out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, as_stream(stream)) !=
+        cudaSuccess)
+        return FP8BS_ERR_CUDA;
+    return status_of(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), as_stream(stream)));
+}
+
+int fp8bs_trace_read(void* host_dst, size_t bytes) {
+    static_assert(FP8BS_TRACE_CALLS == kTraceCalls && FP8BS_TRACE_CTAS == kTraceCtas &&
+                      FP8BS_TRACE_POINTS == kTracePoints,
+                  "fp8bs.h states the trace layout");
+    if (!host_dst) return FP8BS_ERR_ARG;
+    const cudaError_t e = trace_copy(host_dst, bytes);
+    if (e == cudaErrorNotSupported) return FP8BS_ERR_ARG;
+    return status_of(e);
 }
 
 int fp8bs_check_error(void* workspace, void* stream) {

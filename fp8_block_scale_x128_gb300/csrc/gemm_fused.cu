@@ -5,109 +5,123 @@
 //   xq, xs = 1x128-group quant of bf16 x (row amax, scale, e4m3fn codes)
 //   Y[m,n] = bf16( sum_kb P[n,m,kb] * (xs[m,kb] * ws[n/128,kb]) ),
 //   P[n,m,kb] = sum_{k in kb} wq[n,k] * xq[m,k]
-// in one launch.  The page's gfx950 design (per-wave MFMA over a preshuffled
-// weight, each wave quantising its own activations, LDS reduction) is prior
-// art; this is the GB300 form of the same computation.
+// in one launch; with power-of-two (ue8m0) scales the scales are applied
+// inside the MMA ("[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for dense
+// 128x128 fp8 linears (6/8)", "Modifications").  The page's gfx950 design
+// (per-wave MFMA over a preshuffled weight, each wave quantising its own
+// activations, LDS reduction) is prior art; this is the GB300 form.
 //
 // Work unit: one (n-tile of 128 weight rows, 128-wide K block) = one 16 KB fp8
-// weight tile.  The T = N/128 * K/128 units, in n-major order, are split evenly
-// over at most one CTA per SM ("stream-K"): CTA c owns units [c*T/G, (c+1)*T/G),
-// at most 10-12.  A CTA needs about 110 KB of shared memory and 128 registers
-// per thread, so two fit on an SM: with programmatic dependent launch the next
-// call's CTAs stream their weights while this call's CTAs finish.
+// weight tile.  The T = N/128 * K/128 units, in n-major order, are split
+// evenly over at most one CTA per SM ("stream-K"): CTA c owns units
+// [c*T/G, (c+1)*T/G), at most 10-12.  Two CTAs fit on an SM (up to 32
+// tokens), so under programmatic dependent launch the next call's CTAs stream
+// their weights while this call's CTAs finish.
 //   1. Weight ring: one thread keeps 4-5 tiles in flight with bulk async
-//      copies (TMA, evict-first), refilling a slot as soon as the MMAs that
-//      read it complete.  At entry, before the wait for the previous kernel
-//      (they read only the packed weight), the first tiles go to the ring and
-//      the rest of the CTA's tiles are prefetched into L2, so the whole weight
-//      stream starts at once and the refills hit L2.
-//   2. Activations into the shared-memory B operands (K-major, 128-byte
-//      swizzle), for all of the CTA's units:
-//        - up to 6 tokens every CTA quantises its own units' groups;
-//        - above that each 1x128 group is quantised once, by one CTA, and
-//          published in the workspace as 64-bit words that each carry 32 bits
-//          of data (4 codes or the scale) and the call's epoch, with no fence
-//          or flag; a CTA reads the words of its units' groups, re-reads the
-//          ones that still carry an older epoch, and stores the codes into
-//          its operands (a 64-bit access is single-copy atomic, so a word is
-//          either old or wholly new);
-//        - with caller-quantised input the codes and scales are copied with
-//          cp.async.
-//   3. Two threads (even and odd units) issue, per unit, four tcgen05.mma
-//      kind::f8f6f4 (K = 32 each) with the weight tile as the 128-row A
-//      operand and the tokens as N = 16 or 32 ("swap-AB"), into one of 4 TMEM
-//      accumulator stages, and one commit that both frees the ring slot and
-//      publishes the result.
-//   4. Four epilogue warps (one per 32 TMEM lanes) read each accumulator,
-//      free its stage, and accumulate P * (xs[m,kb] * ws[nt,kb]) in fp32
-//      registers (the per-K-block rescale of the page).
-//   5. An n-tile whose whole K range the CTA owns is written as bf16 Y.
-//      Otherwise the tile's first CTA reduces it: each later contributor
-//      writes its partial into its slot, either as tagged words (up to 12
-//      tokens; no fence, no flag) or as fp32 followed by the slot's flags; the
-//      reducer gathers the partials (polled words, or cp.async once the flags
-//      are set) and sums them in CTA order -- a fixed order, so results are
-//      deterministic -- and writes bf16 Y.
+//      copies (TMA, evict-first) and prefetches the CTA's other tiles into
+//      L2, all before the wait for the previous kernel; a slot is refilled as
+//      soon as the MMAs that read it complete.
+//   2. Every CTA quantises the 1x128 groups of the K blocks its units touch
+//      (one "slot" per distinct K block, shared by units of equal K block),
+//      straight into the shared-memory B operands (K-major, 128-byte
+//      swizzle), K block by K block so the MMAs can start on the first.  The
+//      quant code first runs once on dummy data, before the wait, so that
+//      afterwards the instructions and parameters it uses are cached and only
+//      the x loads are cold.  With caller-quantised input the codes and
+//      scales are copied with cp.async instead.
+//   3. One thread issues the MMAs, the weight tile as the 128-row A operand
+//      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each:
+//        fp32 scales: four tcgen05.mma kind::f8f6f4 per unit into one of 4
+//        TMEM stages; four epilogue warps read each stage and accumulate
+//        P * (xs * ws) in fp32 registers (the page's per-K-block rescale);
+//        ue8m0 scales: kind::mxf8f6f4.block_scale MMAs whose per-32 scale
+//        factors sit in TMEM -- each 128-group scale replicated over its four
+//        32-blocks -- accumulating a tile's K range in one TMEM stage, read
+//        once per tile.
+//   4. Split-K: a tile whose K range the CTA owns whole goes straight to bf16
+//      Y.  Otherwise the tile's contributors (consecutive CTAs) share the
+//      reduction by columns: the last contributor -- the one that reaches the
+//      tile first, at the start of its range -- publishes its whole partial;
+//      every other contributor publishes the columns it does not own and
+//      gathers the columns it owns from the others, summing them in CTA order
+//      (a fixed order, so results are deterministic) before writing bf16 Y.
+//      Partials travel as 64-bit words (fp32 bits | the call's epoch) with
+//      plain relaxed stores and no fence or flag; a reader re-reads the words
+//      that still carry an older epoch.
 // A call's epoch is one more than the workspace's epoch word for the CTA's
-// index; every CTA moves the words of its index class on to it when it ends,
-// so all words stay equal and every word or flag of an earlier call is older.
-// Every wait is bounded; on expiry the kernel records FP8BS_ERR_TIMEOUT in the
-// workspace error word, drains its own copies and MMAs (again bounded), frees
-// TMEM and returns.  The code of each role is kept small (rolled loops): the
-// instruction footprint, not the arithmetic, bounds these short phases.
+// index (0 is skipped, so a never-written word never matches); every CTA moves
+// the words of its index class on to it when it ends.  Every wait is bounded;
+// on expiry the kernel records FP8BS_ERR_TIMEOUT in the workspace error word,
+// drains its own copies and MMAs (again bounded), frees TMEM and returns.
+#include <atomic>
+
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace fp8bs {
 namespace {
 
-// 8 warps.  Warp 0: weight ring (one thread).  Warps 1 and 3: MMA issue (one
-// thread each, even and odd units: one thread cannot keep the tensor pipe
-// fed); warp 1 also owns TMEM, warp 3 first builds the scale table.  Warp 2:
-// unit info and header check, then quant.  Warps 4-7: quant, then the
-// epilogue (one warp per 32 TMEM lanes).
-constexpr int kThreads = 256;
-constexpr int kQuantThreads = 160;  // warps 2 and 4-7
-constexpr int kQuantHalfWarps = kQuantThreads / 16;
-constexpr int kLocalMaxM = 6;  // up to this many tokens every CTA quantises its own groups
-constexpr int kAccStages = 4;
+#ifdef FP8BS_TRACE
+__device__ unsigned long long g_trace[kTraceCalls * kTraceCtas * kTracePoints * 2];
+#endif
 
-// Where a CTA's activation codes come from.
+// 8 warps.  Warp 0: weight ring (one thread) and quant.  Warp 1: MMA issue
+// (one thread) and TMEM.  Warp 2: unit info and header check, then quant.
+// Warp 3: scale table, then quant.  Warps 4-7: quant, then the epilogue (one
+// warp per 32 TMEM lanes).
+constexpr int kThreads = 256;
+constexpr int kQuantHalfWarps = 14;  // warps 0 and 2-7
+constexpr int kQuantThreads = 16 * kQuantHalfWarps;
+constexpr int kQuantDepth = 4;       // groups per half-warp with their x loads in flight
+
+// Where the activation codes come from.
 enum : int {
-    kSrcLocal = 0,     // every CTA quantises its own units' groups (few tokens)
-    kSrcExchange = 1,  // each group quantised once, exchanged through the workspace
-    kSrcInput = 2,     // codes and scales given by the caller (the two-launch path)
+    kSrcQuant = 0,  // every CTA quantises the groups its units need
+    kSrcInput = 1,  // codes and scales given by the caller (the two-launch path)
 };
 
-// MPAD 16 and 32: two CTAs per SM (the next call's CTAs start while this
-// call's finish); MPAD 64: one CTA per SM with a deeper weight ring.
-template <int MPAD, int SRC>
+template <int MPAD, int KIND>
 struct Cfg {
     static constexpr int kCtasPerSm = MPAD == 64 ? 1 : 2;
     static constexpr uint32_t kMaxSmem = MPAD == 64 ? 227 * 1024 : 112 * 1024;
     static constexpr int kUnits = MPAD == 16 ? kMaxUnitsM16 : (MPAD == 32 ? kMaxUnitsM32 : kMaxUnitsM64);
     static constexpr int kStages = MPAD == 16 ? 5 : (MPAD == 32 ? 4 : 8);
-    static constexpr uint32_t kBBytes = MPAD * 128;  // activation operand of one unit
-    static constexpr uint32_t kTmemCols = kAccStages * MPAD;
+    static constexpr uint32_t kBBytes = MPAD * 128;  // activation operand of one K block
+    // TMEM accumulator stages: fp32 scales, one per unit -- as many as fit, so
+    // the MMAs rarely wait for the epilogue; ue8m0, one per tile segment
+    static constexpr int kAcc = KIND == FP8BS_SCALE_UE8M0 ? 4 : (MPAD == 16 ? 12 : 8);
+    // then (ue8m0) the scale factors, every scale-factor address on a
+    // 4-column boundary: 4 columns per unit for the weight (one per lane
+    // quadrant) and 4 per K block for the tokens (MPAD/32 of them used)
+    static constexpr uint32_t kSfaCol = kAcc * MPAD;
+    static constexpr uint32_t kSfbCols = MPAD > 32 ? 2 : 1;
+    static constexpr uint32_t kSfbCol = kSfaCol + 4 * kUnits;
+    static constexpr uint32_t kTmemUsed = KIND == FP8BS_SCALE_UE8M0 ? kSfbCol + 4 * kUnits : kSfaCol;
+    static constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
     static constexpr uint32_t kRingBytes = kStages * kTileBytes;
     static constexpr uint32_t kOffB = kRingBytes;
-    static constexpr uint32_t kOffXs = kOffB + kUnits * kBBytes;
+    static constexpr uint32_t kOffXs = kOffB + kUnits * kBBytes;  // [slot][MPAD] fp32 scale bits or e8m0 bytes
     static constexpr uint32_t kOffWs = kOffXs + kUnits * MPAD * 4;
-    static constexpr uint32_t kOffKb = kOffWs + kUnits * 4;
-    static constexpr uint32_t kOffTab = (kOffKb + kUnits * 4 + 15) / 16 * 16;
+    static constexpr uint32_t kOffTab = (kOffWs + kUnits * 4 + 15) / 16 * 16;
     static constexpr uint32_t kOffBar = kOffTab + kScaleTab * 8;
-    // full[S], empty[S], acce[A], bready[U], hdr
-    static constexpr uint32_t kNumBars = 2 * kStages + kAccStages + kUnits + 1;
+    // full[S], empty[S], acce[A], accfull[A], bready[U], hdr, sfready
+    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kAcc + kUnits + 2;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+#ifdef FP8BS_TRACE
+    static constexpr uint32_t kOffTrace = kOffMisc + 64;  // timeline record (traced builds only)
+    static constexpr uint32_t kSmem = kOffTrace + kTracePoints * 16 + 1024;
+#else
     static constexpr uint32_t kSmem = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
-    // local quant: groups (unit, token) per half-warp
-    static constexpr int kGroupsPerHw = (kUnits * kLocalMaxM + kQuantHalfWarps - 1) / kQuantHalfWarps;
-    // exchange: groups (unit, token) per quantising thread
-    static constexpr int kGroupsPerThread = (kUnits * MPAD + kQuantThreads - 1) / kQuantThreads;
+#endif
+    // the gather stage of one epilogue warp: its quarter of the (idle) ring
+    static constexpr uint32_t kStageFloats = kRingBytes / 16;
     static_assert(kSmem <= kMaxSmem, "shared memory per CTA");
     static_assert(MPAD == 16 || MPAD == 32 || MPAD == 64, "token tile");
     static_assert(kBBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
-    static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
+    static_assert(kTmemUsed <= kTmemCols && kTmemCols * kCtasPerSm <= 512, "TMEM allocation");
+    static_assert(kSfaCol % 4 == 0 && kSfbCol % 4 == 0, "scale-factor columns on 4-column boundaries");
+    static_assert(kStageFloats >= 2 * MPAD * 32 + 32 * ((kMaxCtas + 31) / 32), "gather stage");
 };
 
 struct Params {
@@ -123,9 +137,7 @@ struct Params {
     int64_t ldy;
     uint32_t* err;
     uint32_t* gen;            // epoch words
-    uint32_t* pflag;          // partial flags [CTA][4 epilogue warps]
-    uint64_t* slots;          // partial slots, 32 KB per CTA: [32 cols][128 rows] tagged or [64][128] fp32
-    uint8_t* act;             // activation records [K/128][kKbRecBytes]
+    uint64_t* slots;          // partial slots: [CTA][2][64 columns][128 rows] tagged words
     uint8_t* xq_out;
     void* xs_out;
     const uint8_t* xq_in;     // kSrcInput: codes [M][ldxq], scales [M][K/128]
@@ -135,7 +147,6 @@ struct Params {
     int pdl;
 };
 
-// kMiscCommitted + 0 / + 1: units committed by the even / odd MMA issuer
 enum : int { kMiscTmem = 0, kMiscAbort = 1, kMiscHdrOk = 2, kMiscIssued = 3, kMiscCommitted = 4 };
 
 __device__ __forceinline__ uint32_t unit_begin(uint32_t c, uint32_t T, uint32_t G) {
@@ -155,26 +166,12 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
     return r;
 }
 
-// Activation words of K block kb: scales [32 rows], codes [32 rows][32 words].
-__device__ __forceinline__ uint64_t* kb_scales(const Params& p, uint32_t kb) {
-    return reinterpret_cast<uint64_t*>(p.act + kb * kKbRecBytes + kKbRecScales);
-}
-__device__ __forceinline__ uint64_t* kb_codes(const Params& p, uint32_t kb) {
-    return reinterpret_cast<uint64_t*>(p.act + kb * kKbRecBytes + kKbRecCodes);
-}
-
 __device__ __forceinline__ uint64_t tag(uint32_t data, uint32_t epoch) {
     return static_cast<uint64_t>(data) | (static_cast<uint64_t>(epoch) << 32);
 }
 __device__ __forceinline__ bool tagged(uint64_t w, uint32_t epoch) { return static_cast<uint32_t>(w >> 32) == epoch; }
 
 // Single-copy-atomic 64-bit exchange words (relaxed, GPU scope).
-__device__ __forceinline__ void st_pair(uint64_t* p, uint64_t a, uint64_t b) {
-    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
-}
-__device__ __forceinline__ void ld_pair(const uint64_t* p, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
 __device__ __forceinline__ void st_word(uint64_t* p, uint64_t a) {
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
 }
@@ -205,15 +202,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const P
     return true;
 }
 
-// Bookkeeping of a bounded poll begun at t0: true once the CTA has aborted,
-// or (recorded) once the wait has run past the limit.
-__device__ __forceinline__ bool gave_up(long long t0, const Params& p, volatile uint32_t* misc) {
-    if (misc[kMiscAbort] != 0) return true;
-    if (clock64() - t0 > p.timeout) {
-        raise_timeout(p.err, misc);
-        return true;
-    }
-    return false;
+// The same wait for a whole warp (lane 0 polls); false if it gave up.
+__device__ __forceinline__ bool warp_wait_bar(uint64_t* bar, uint32_t parity, const Params& p, volatile uint32_t* misc,
+                                              int lane) {
+    uint32_t ok = 0;
+    if (lane == 0) ok = wait_bar(bar, parity, p, misc) ? 1u : 0u;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 // Teardown drain: ignores the abort flag, still bounded.
@@ -223,154 +217,138 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, long long
     }
 }
 
-// Bounded wait until a flag carries the epoch (acquire), by one thread.
-__device__ __forceinline__ bool wait_flag(const uint32_t* f, uint32_t epoch, const Params& p, volatile uint32_t* misc) {
-    if (ptx::ld_acquire_u32(f) == epoch) return true;
-    const long long t0 = clock64();
-    while (ptx::ld_acquire_u32(f) != epoch) {
-        if (misc[kMiscAbort] != 0) return false;
-        if (clock64() - t0 > p.timeout) {
-            raise_timeout(p.err, misc);
-            return false;
-        }
-    }
-    return true;
+// Word offset (from p.slots) of CTA b's partial slot for n-tile nt: slot 0
+// if nt is the tile of b's first unit, else slot 1 (its last tile).
+__device__ __forceinline__ uint32_t slot_offset(const Params& p, uint32_t b, uint32_t nt, uint32_t G) {
+    const uint32_t which = unit_begin(b, p.T, G) / static_cast<uint32_t>(p.KB) == nt ? 0u : 1u;
+    return (b * kSlotsPerCta + which) * static_cast<uint32_t>(kSlotWords);
 }
 
+// Output of one n-tile segment by one epilogue warp: its 32 rows r = q*32 +
+// lane, acc = this CTA's partial sums of them.  c0..c1: the tile's
+// contributors (consecutive CTAs), c this CTA.  Returns false if a wait gave up.
+//   c0 == c1: the whole K range is here -> bf16 Y.
+//   c == c1:  the last contributor (it reached the tile at the start of its
+//             range) publishes every column and owns none.
+//   else:     contributor s = c - c0, one of the S - 1 owners, owns columns
+//             [s*M/(S-1), (s+1)*M/(S-1)): it publishes the others, then gathers
+//             its own from the other contributors (rounds of loads in flight,
+//             the stale words re-read until they carry the epoch) and sums
+//             each column in CTA order, its own partial at its place.
+// An owner's segment is always the last of its CTA's range, so the ring is
+// idle and its quarter q serves as the stage: the other contributors' slot
+// offsets, then its own values and the running sums of the owned columns.
 template <int MPAD>
-__device__ __forceinline__ void store_y(const Params& p, int n, const float (&v)[MPAD]) {
+__device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, const float (&acc)[MPAD], uint32_t c,
+                                              uint32_t c0, uint32_t c1, uint32_t G, int q, int lane, uint32_t epoch,
+                                              volatile uint32_t* misc, float* stage) {
+    const int r = q * 32 + lane;
+    uint16_t* yrow = p.y + static_cast<size_t>(nt) * kTile + r;
+    if (c0 == c1) {
+#pragma unroll
+        for (int m = 0; m < MPAD; ++m)
+            if (m < p.M) yrow[m * p.ldy] = f32_to_bf16_rn(acc[m]);
+        return true;
+    }
+    const int owners = static_cast<int>(c1 - c0);
+    const int s = static_cast<int>(c - c0);
+    const int m_lo = c == c1 ? p.M : s * p.M / owners;
+    const int m_hi = c == c1 ? p.M : (s + 1) * p.M / owners;
+    uint64_t* mine = p.slots + slot_offset(p, c, nt, G) + r;
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
-        if (m < p.M) p.y[m * p.ldy + n] = f32_to_bf16_rn(v[m]);
-}
-
-// Calls of up to this many tokens exchange split-K partials as tagged words;
-// larger ones as fp32 with a flag per epilogue warp.  A tagged reader needs
-// one round of loads per kTaggedRound words, a flagged one a single wait and
-// one copy, plus the writer's fence.
-constexpr int kTaggedMaxM = 12;
-constexpr int kTaggedRound = 16;
-
-// Word of the partial (contributor b + t / M, column t % M, row r).
-__device__ __forceinline__ const uint64_t* partial_word(const Params& p, uint32_t b, int t, int r) {
-    const int j = static_cast<int>(div_m(static_cast<uint32_t>(t), p.mdiv));
-    const int m = t - j * p.M;
-    return p.slots + static_cast<size_t>(b + j) * (32 * 128) + m * 128 + r;
-}
-
-__device__ __forceinline__ float* fp32_slot(const Params& p, uint32_t b) {
-    return reinterpret_cast<float*>(p.slots + static_cast<size_t>(b) * (32 * 128));
-}
-
-// Output of one n-tile's accumulator by one epilogue warp (rows q*32 .. +31).
-// role 0: this CTA owns the tile's whole K range -> bf16 Y.
-// role 1: a later contributor -> write the partial of these rows into this
-//         CTA's slot: tagged words (no fence, no flag) or fp32 and then this
-//         warp's flag.
-// role 2: the reducer -> gather the later contributors' partials of these
-//         rows (batches that fit this warp's quarter of the idle weight ring),
-//         sum in CTA order, bf16 Y.  Tagged words are read in rounds of loads
-//         in flight, the stale ones re-read together until they carry the
-//         epoch; fp32 partials are copied (cp.async) once their flags carry it.
-// last: the CTA that holds the tile's last unit.  Returns false if a wait
-// gave up.
-template <int MPAD, int STAGE_FLOATS, bool TAGGED>
-__device__ __forceinline__ bool flush_tile(const Params& p, uint32_t nt, float (&acc)[MPAD], uint32_t c, uint32_t last,
-                                        int role, int q, int lane, uint32_t epoch, volatile uint32_t* misc,
-                                        float* stage) {
-    const int r = q * 32 + lane;
-    const int n = static_cast<int>(nt) * kTile + r;
-    if (role == 0) {
-        store_y<MPAD>(p, n, acc);
-        return true;
+        if (m < p.M && (m < m_lo || m >= m_hi)) st_word(mine + m * kTile, tag(__float_as_uint(acc[m]), epoch));
+    if (m_lo == m_hi) return true;
+#ifdef FP8BS_TRACE
+    if (q == 0 && lane == 0) {
+        volatile unsigned long long* rec = reinterpret_cast<volatile unsigned long long*>(misc + 16);
+        FP8BS_STAMP_CLK(rec, kTpGather);
     }
-    if (role == 1) {
-        if constexpr (TAGGED) {
-            uint64_t* slot = p.slots + static_cast<size_t>(c) * (32 * 128);
+#endif
+    const int width = m_hi - m_lo;
+    uint32_t* tab = reinterpret_cast<uint32_t*>(stage);  // [owners] other contributors' slot offsets
+    float* own = stage + (owners + 31) / 32 * 32;       // [width][32]
+    float* sum = own + width * 32;                      // [width][32]
+#pragma unroll 1
+    for (int j = lane; j < owners; j += 32) {
+        const uint32_t b = c0 + static_cast<uint32_t>(j) + (c0 + static_cast<uint32_t>(j) >= c ? 1u : 0u);
+        tab[j] = slot_offset(p, b, nt, G) + static_cast<uint32_t>(m_lo * kTile);
+    }
 #pragma unroll
-            for (int m = 0; m < MPAD; ++m)
-                if (m < p.M) st_word(slot + m * 128 + r, tag(__float_as_uint(acc[m]), epoch));
-        } else {
-            float* slot = fp32_slot(p, c);
-#pragma unroll
-            for (int m = 0; m < MPAD; ++m)
-                if (m < p.M) slot[m * 128 + r] = acc[m];
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) ptx::st_release_u32(p.pflag + c * 4 + q, epoch);
+    for (int m = 0; m < MPAD; ++m)
+        if (m >= m_lo && m < m_hi) {
+            own[(m - m_lo) * 32 + lane] = acc[m];
+            sum[(m - m_lo) * 32 + lane] = 0.0f;
         }
-        return true;
-    }
-    const int per = p.M * 32;               // floats per contributor (this warp's rows)
-    const int batch = STAGE_FLOATS / per;   // contributors per batch (>= 4)
-    float* st = stage + q * STAGE_FLOATS;   // this warp's quarter of the ring
+    __syncwarp();
+    // word t = j * width + col: column m_lo + col of the j-th other contributor
+    const int nw = owners * width;
+    constexpr int kRound = 16;
+    bool ok = true;
 #pragma unroll 1
-    for (uint32_t b = c + 1; b <= last; b += batch) {
-        const int nb = static_cast<int>(last + 1 - b) < batch ? static_cast<int>(last + 1 - b) : batch;
-        bool ok = true;
-        if constexpr (TAGGED) {
-            const int nw = nb * p.M;        // this lane's words: t = j * M + m
-#pragma unroll 1
-            for (int base = 0; base < nw && ok; base += kTaggedRound) {
-                uint64_t w[kTaggedRound];
+    for (int base = 0; base < nw && ok; base += kRound) {
+        uint32_t off[kRound];
+        uint64_t w[kRound];
+        int j = base / width, col = base - j * width;
 #pragma unroll
-                for (int k = 0; k < kTaggedRound; ++k)
-                    w[k] = base + k < nw ? ld_word(partial_word(p, b, base + k, r)) : tag(0, epoch);
-                const long long t0 = clock64();
-                while (true) {
-                    bool all = true;
-#pragma unroll
-                    for (int k = 0; k < kTaggedRound; ++k) all = all && tagged(w[k], epoch);
-                    if (all) break;
-                    if (gave_up(t0, p, misc)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int k = 0; k < kTaggedRound; ++k)
-                        if (!tagged(w[k], epoch)) w[k] = ld_word(partial_word(p, b, base + k, r));
-                }
-#pragma unroll
-                for (int k = 0; k < kTaggedRound; ++k)
-                    if (base + k < nw) st[(base + k) * 32 + lane] = __uint_as_float(static_cast<uint32_t>(w[k]));
+        for (int k = 0; k < kRound; ++k) {
+            off[k] = base + k < nw ? tab[j] + static_cast<uint32_t>(col * kTile + r) : 0u;
+            w[k] = base + k < nw ? ld_word(p.slots + off[k]) : tag(0, epoch);
+            if (++col == width) {
+                col = 0;
+                ++j;
             }
-            if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-        } else {
-            if (lane < nb) ok = wait_flag(p.pflag + (b + lane) * 4 + q, epoch, p, misc);
-            if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-            // 16-byte chunks: (contributor j, column m, rows 4k .. 4k+3 of this warp)
-#pragma unroll 1
-            for (int t = lane; t < nb * p.M * 8; t += 32) {
-                const int jm = t >> 3, k = t & 7;
-                const int j = jm / p.M;
-                const int m = jm - j * p.M;
-                ptx::cp_async16(st + jm * 32 + 4 * k, fp32_slot(p, b + j) + m * 128 + q * 32 + 4 * k);
-            }
-            ptx::cp_async_wait_all();
         }
-        __syncwarp();
-#pragma unroll 1
-        for (int j = 0; j < nb; ++j) {
+        const long long t0 = clock64();
+        while (true) {
+            bool all = true;
 #pragma unroll
-            for (int m = 0; m < MPAD; ++m)
-                if (m < p.M) acc[m] += st[(j * p.M + m) * 32 + lane];
+            for (int k = 0; k < kRound; ++k) all = all && tagged(w[k], epoch);
+            if (all) break;
+            if (misc[kMiscAbort] != 0) {
+                ok = false;
+                break;
+            }
+            if (clock64() - t0 > p.timeout) {
+                raise_timeout(p.err, misc);
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int k = 0; k < kRound; ++k)
+                if (!tagged(w[k], epoch)) w[k] = ld_word(p.slots + off[k]);
         }
-        __syncwarp();
+        // running sums in CTA order: the own partial enters just before the
+        // first other contributor that follows this CTA (j == s)
+        j = base / width;
+        col = base - j * width;
+#pragma unroll
+        for (int k = 0; k < kRound; ++k) {
+            if (base + k < nw) {
+                float v = sum[col * 32 + lane];
+                if (j == s) v += own[col * 32 + lane];
+                sum[col * 32 + lane] = v + __uint_as_float(static_cast<uint32_t>(w[k]));
+            }
+            if (++col == width) {
+                col = 0;
+                ++j;
+            }
+        }
     }
-    store_y<MPAD>(p, n, acc);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+#pragma unroll 1
+    for (int col = 0; col < width; ++col) yrow[(m_lo + col) * p.ldy] = f32_to_bf16_rn(sum[col * 32 + lane]);
     return true;
 }
 
-// Store one quantised slice (unit i, row m, 16-byte part l16) into the B
-// operand, the group scale into sXs, then arrive on unit i's barrier.
-template <int MPAD>
-__device__ __forceinline__ void put_slice(uint8_t* sB, float* sXs, uint64_t* bready, int i, int m, int l16,
-                                          uint32_t lo, uint32_t hi, float scale) {
+// Store one quantised slice (K-block slot i, row m, 16-byte part l16) into the
+// B operand and the group scale into sXs (the caller then fences and arrives
+// on slot i's barrier).
+template <int MPAD, int KIND>
+__device__ __forceinline__ void put_slice(uint8_t* sB, uint32_t* sXs, int i, int m, int l16, const SliceQuant& qs) {
     uint8_t* row = sB + i * (MPAD * 128) + (m >> 3) * 1024 + (m & 7) * 128;
-    *reinterpret_cast<uint2*>(row + (((l16 >> 1) ^ (m & 7)) << 4) + ((l16 & 1) << 3)) = make_uint2(lo, hi);
-    if (l16 == 0) sXs[i * MPAD + m] = scale;
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(&bready[i]);
+    *reinterpret_cast<uint2*>(row + (((l16 >> 1) ^ (m & 7)) << 4) + ((l16 & 1) << 3)) = make_uint2(qs.lo, qs.hi);
+    if (l16 == 0) sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale);
 }
 
 template <int KIND>
@@ -386,25 +364,35 @@ __device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t
     }
 }
 
-template <int MPAD, int KIND, int SRC, bool TAGGED>
-__global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
+template <int MPAD, int KIND, int SRC>
+__global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
     fused_quant_gemm_kernel(const __grid_constant__ Params p) {
-    using C = Cfg<MPAD, SRC>;
+    using C = Cfg<MPAD, KIND>;
     constexpr int S = C::kStages;
+    constexpr int NA = C::kAcc;
+    constexpr bool kBlockScaled = KIND == FP8BS_SCALE_UE8M0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sRing = smem;
     uint8_t* sB = smem + C::kOffB;
-    float* sXs = reinterpret_cast<float*>(smem + C::kOffXs);
+    uint32_t* sXs = reinterpret_cast<uint32_t*>(smem + C::kOffXs);
     float* sWs = reinterpret_cast<float*>(smem + C::kOffWs);
-    int* sKb = reinterpret_cast<int*>(smem + C::kOffKb);
     float2* sTab = reinterpret_cast<float2*>(smem + C::kOffTab);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* empty = full + S;  // completes when the MMAs that read the slot are done
-    uint64_t* acce = empty + S;
-    uint64_t* bready = acce + kAccStages;
+    uint64_t* acce = empty + S;      // an accumulator stage has been read
+    uint64_t* accfull = acce + NA;   // an accumulator stage holds its unit's (ue8m0: segment's) sum
+    uint64_t* bready = accfull + NA;
     uint64_t* hdr_bar = bready + C::kUnits;  // completes once misc[kMiscHdrOk] is written
+    uint64_t* sf_bar = hdr_bar + 1;          // ue8m0: the token scale factors are in TMEM
     volatile uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+#ifdef FP8BS_TRACE
+    volatile unsigned long long* trec = reinterpret_cast<unsigned long long*>(smem + C::kOffTrace);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * kTracePoints; ++i) trec[i] = 0;
+        FP8BS_STAMP(trec, kTpEntry);
+    }
+#endif
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t G = gridDim.x, c = blockIdx.x;
@@ -412,23 +400,27 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
     const int cnt = static_cast<int>(u1 - u0);
     const uint32_t KB = static_cast<uint32_t>(p.KB);
     const uint32_t nt0 = u0 / KB, kb0 = u0 - nt0 * KB;
+    // K-block slots: unit i uses slot i % KB (the range's distinct K blocks)
+    const int nslots = cnt < p.KB ? cnt : p.KB;
 
     // ---- set-up; the first ring tiles go out at once ---------------------------
     if (tid == 0) {
-        // arrivals per unit: one per 16-byte code slice (local quant), one per
-        // 8-code chunk and one per scale (exchange), or one per copied group
-        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (SRC == kSrcLocal ? 16 : (SRC == kSrcExchange ? 17 : 1));
+        // arrivals per slot: one per 16-byte code slice (quant) or per copied group
+        const uint32_t arrivals = static_cast<uint32_t>(p.M) * (SRC == kSrcQuant ? 16 : 1);
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < kAccStages; ++a) ptx::mbar_init(&acce[a], 4);
-        for (int i = 0; i < cnt; ++i) ptx::mbar_init(&bready[i], arrivals);
+        for (int a = 0; a < NA; ++a) {
+            ptx::mbar_init(&acce[a], 4);
+            ptx::mbar_init(&accfull[a], 1);
+        }
+        for (int i = 0; i < nslots; ++i) ptx::mbar_init(&bready[i], arrivals);
         ptx::mbar_init(hdr_bar, 1);
+        ptx::mbar_init(sf_bar, 4);
         misc[kMiscAbort] = 0;
         misc[kMiscHdrOk] = 0;
         misc[kMiscCommitted] = 0;
-        misc[kMiscCommitted + 1] = 0;
         ptx::fence_mbar_init();
         const uint64_t pol = ptx::policy_evict_first();
         const int pre = cnt < S ? cnt : S;
@@ -450,18 +442,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
     }
     if (warp == 3) fill_scale_table(sTab, lane, 32);
     if (warp == 2 && lane < cnt) {
-        uint32_t kb = kb0 + lane;
-        while (kb >= KB) kb -= KB;
-        sKb[lane] = static_cast<int>(kb);
-        const uint32_t u = u0 + lane;
-        sWs[lane] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(p.wscales[u])
-                                              : reinterpret_cast<const float*>(p.wscales)[u];
+        const uint32_t u = u0 + static_cast<uint32_t>(lane);
+        sWs[lane] = kBlockScaled ? __uint_as_float(p.wscales[u]) : reinterpret_cast<const float*>(p.wscales)[u];
     }
     if (p.pdl) ptx::griddep_launch_dependents();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[kMiscTmem];
+    if (tid == 0) FP8BS_STAMP(trec, kTpSetup);
 
     if (warp == 2 && lane == 0) {  // packed-weight header check
         const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
@@ -470,15 +459,158 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
         misc[kMiscHdrOk] = ok ? 1u : 0u;
         ptx::mbar_arrive(hdr_bar);  // release: the epilogue reads the flag after waiting here
     }
-    // quantising threads: qt = 0 .. kQuantThreads-1 over warps 2, 4-7
-    const int qt = warp == 2 ? tid - 64 : tid - 96;
+    if (kBlockScaled && warp >= 4) {
+        // weight scale factors: unit i's e8m0 byte in all four bytes of TMEM
+        // column kSfaCol + 4i + q for the rows of quadrant q (row r reads lane
+        // r, column base + r/32)
+        const int q = warp & 3;
+#pragma unroll 1
+        for (int i = 0; i < cnt; ++i) {
+            const uint32_t b = __float_as_uint(sWs[i]) & 0xFFu;
+            ptx::tmem_st_32x32b_x1(tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kSfaCol + 4 * i + q,
+                                   b * 0x01010101u);
+        }
+        ptx::tmem_wait_st();
+    }
+    const bool quant_warp = warp != 1;
+    const int qt = warp == 0 ? tid : tid - 32;  // quantising threads 0..223
     const int hw = qt >> 4;
     const int l16 = qt & 15;
     const int hw_first = hw & ~1;  // the warp's first half-warp
-    // Everything below may read what the previous kernel on the stream wrote.
-    if (p.pdl) ptx::griddep_wait();
+    uint32_t epoch = 0;
+
+    if (SRC == kSrcQuant && quant_warp) {
+        // ---- 2. quantise the groups of this CTA's K-block slots -------------------
+        // group g = slot * M + m (slot-major, so slot 0 is ready first); the
+        // half-warp's t-th group is g = hw + 14 t, in rounds of kQuantDepth:
+        // a round first issues the x loads of the next round, then quantises
+        // its own groups, so one round of work covers the load latency.  Pass
+        // 0 runs one round of this code on dummy values before the wait,
+        // writing nothing.
+        const int ng = nslots * p.M;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                if (p.pdl) ptx::griddep_wait();
+                if (tid == 64) FP8BS_STAMP(trec, kTpWait);
+                epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
+                if (epoch == 0) epoch = 1;
+            }
+            uint4 raw[kQuantDepth], nxt[kQuantDepth];
+#pragma unroll
+            for (int k = 0; k < kQuantDepth; ++k) {
+                const int g = hw + kQuantHalfWarps * k;
+                raw[k] = make_uint4(0x3F8A3F81u + k, 0x3F933FA5u, 0xBF853F99u, 0x3FC13F87u);
+                if (pass == 1 && g < ng) {
+                    const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
+                    const uint32_t kb = (kb0 + i) % KB;
+                    raw[k] = ptx::ld_global_v4(p.x + m * p.ldx + kb * kTile + l16 * 8);
+                }
+            }
+            if (pass == 1 && tid == 64) FP8BS_STAMP_AFTER(trec, kTpXload, raw[0].x);
+            uint32_t sink = 0;
+#pragma unroll 1
+            for (int t0 = 0; pass == 0 ? t0 == 0 : hw_first + kQuantHalfWarps * t0 < ng; t0 += kQuantDepth) {
+                // the next round's loads first; then the round's kQuantDepth
+                // groups: quantise all (independent chains the compiler can
+                // interleave), store codes and scales, one proxy fence, the
+                // arrivals
+#pragma unroll
+                for (int k = 0; k < kQuantDepth; ++k) {
+                    const int g2 = hw + kQuantHalfWarps * (t0 + k + kQuantDepth);
+                    nxt[k] = raw[k];
+                    if (pass == 1 && g2 < ng) {
+                        const uint32_t i2 = div_m(static_cast<uint32_t>(g2), p.mdiv), m2 = g2 - i2 * p.M;
+                        const uint32_t kb2 = (kb0 + i2) % KB;
+                        nxt[k] = ptx::ld_global_v4(p.x + m2 * p.ldx + kb2 * kTile + l16 * 8);
+                    }
+                }
+                SliceQuant qs[kQuantDepth];
+#pragma unroll
+                for (int k = 0; k < kQuantDepth; ++k) {
+                    qs[k].lo = qs[k].hi = 0;
+                    if (pass == 0 || hw_first + kQuantHalfWarps * (t0 + k) < ng) qs[k] = quant_slice<KIND>(raw[k], sTab);  // warp-uniform
+                    sink ^= qs[k].lo;
+                }
+                if (pass == 1) {
+#pragma unroll
+                    for (int k = 0; k < kQuantDepth; ++k) {
+                        const int g = hw + kQuantHalfWarps * (t0 + k);
+                        if (g < ng) {
+                            const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
+                            if (u0 + i < KB) put_xq_out<KIND>(p, m, u0 + i, l16, qs[k]);  // n-tile 0 publishes xq / xs
+                            put_slice<MPAD, KIND>(sB, sXs, static_cast<int>(i), static_cast<int>(m), l16, qs[k]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+#pragma unroll
+                    for (int k = 0; k < kQuantDepth; ++k) {
+                        const int g = hw + kQuantHalfWarps * (t0 + k);
+                        if (g < ng) ptx::mbar_arrive(&bready[div_m(static_cast<uint32_t>(g), p.mdiv)]);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kQuantDepth; ++k) raw[k] = nxt[k];
+                if (pass == 1 && t0 == 0 && tid == 64) FP8BS_STAMP_CLK(trec, kTpQuantFirst);
+            }
+            asm volatile("" ::"r"(sink));
+        }
+        if (tid == 64) FP8BS_STAMP_CLK(trec, kTpQuantDone);
+    } else {
+        if (p.pdl) ptx::griddep_wait();
+        if (tid == 64) FP8BS_STAMP(trec, kTpWait);
+        if (quant_warp) {
+            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
+            if (epoch == 0) epoch = 1;
+        }
+    }
     if (warp == 2 && lane == 0 && misc[kMiscHdrOk] == 0) record_error(p.err, FP8BS_ERR_SCALE_KIND);
-    uint32_t epoch = 0;  // read by the quantising threads, after their x loads are in flight
+
+    if (SRC == kSrcInput && quant_warp) {
+        // ---- 2'. the caller's codes and scales of this CTA's K-block slots -------
+        // group g = slot * M + m; thread qt takes g = qt + 224 j: all copies in
+        // flight, then one wait.
+        const int ng = nslots * p.M;
+#pragma unroll 1
+        for (int g = qt; g < ng; g += kQuantThreads) {
+            const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
+            const uint32_t kb = (kb0 + i) % KB;
+            const uint8_t* src = p.xq_in + m * p.ldxq + kb * kTile;
+            uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) ptx::cp_async16(row + ((ch ^ (m & 7)) << 4), src + ch * 16);
+            sXs[i * MPAD + m] = kBlockScaled ? static_cast<const uint8_t*>(p.xs_in)[m * p.KB + kb]
+                                             : static_cast<const uint32_t*>(p.xs_in)[m * p.KB + kb];
+        }
+        ptx::cp_async_wait_all();
+        if (tid == 64) FP8BS_STAMP_CLK(trec, kTpXchgDone);
+        ptx::fence_proxy_async_smem();
+#pragma unroll 1
+        for (int g = qt; g < ng; g += kQuantThreads) ptx::mbar_arrive(&bready[div_m(static_cast<uint32_t>(g), p.mdiv)]);
+    }
+
+    if (kBlockScaled && warp >= 4) {
+        // token scale factors: slot i's e8m0 byte of token n in all four bytes
+        // of lane n % 32 of every quadrant, column kSfbCol + 4i + n/32
+        const int q = warp & 3;
+        bool ok = true;
+#pragma unroll 1
+        for (int i = 0; i < nslots && ok; ++i) {
+            ok = warp_wait_bar(&bready[i], 0, p, misc, lane);
+#pragma unroll
+            for (int h = 0; h < static_cast<int>(C::kSfbCols); ++h) {
+                const int n = h * 32 + lane;
+                const uint32_t b = n < p.M ? sXs[i * MPAD + n] & 0xFFu : 127u;
+                ptx::tmem_st_32x32b_x1(tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kSfbCol + 4 * i + h,
+                                       b * 0x01010101u);
+            }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sf_bar);
+        if (tid == 128) FP8BS_STAMP_CLK(trec, kTpXchgDone);
+    }
 
     if (warp == 0) {
         // ---- 1. weight ring refills ------------------------------------------------
@@ -492,307 +624,193 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
                 ptx::bulk_g2s(sRing + s * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
                               &full[s], pol);
                 misc[kMiscIssued] = static_cast<uint32_t>(i + 1);
+                if (i - S < 8) FP8BS_STAMP_CLK(trec, kTpRefill + i - S);
             }
         }
         __syncwarp();
-    } else if (warp == 1 || warp == 3) {
-        // ---- 3. MMA issue: warp 1 the even units, warp 3 the odd ones -------------
+    } else if (warp == 1) {
+        // ---- 3. MMA issue ----------------------------------------------------------
+        // An mbarrier probe takes ~180 cycles to answer, about half a unit of
+        // MMA time, so the issuer probes in batches: the ring's first tiles
+        // (requested long before) once at the start, and the K-block operands
+        // four at a time; it waits on one barrier only when a batch says not
+        // yet.  The accumulator stages outnumber the units of most CTAs, so
+        // waits for the epilogue are rare.
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
-            const int odd = warp == 3 ? 1 : 0;
+            bool ok = !kBlockScaled || wait_bar(sf_bar, 0, p, misc);
+            uint32_t known = 0;  // bit s: ring slot s holds its first tile; bit 16 + j: slot j's operand is ready
+            for (int s0 = 0; s0 < S && s0 < cnt; s0 += 4)
+                known |= ptx::mbar_test4(&full[s0], 0, &full[(s0 + 1) % S], 0, &full[(s0 + 2) % S], 0,
+                                         &full[(s0 + 3) % S], 0) << s0;
+            uint32_t seg = 0, kb = kb0;  // tile segment of unit i and its K block
+            // nothing is stored to shared memory inside this loop: a generic
+            // store queued behind the MMAs' operand reads was measured to hold
+            // the thread; the count of committed units is stored once, after it
+            int committed = 0;
+#ifdef FP8BS_TRACE
+            long long t_issue[10];
+#endif
 #pragma unroll 1
-            for (int i = odd; i < cnt; i += 2) {
-                const int s = i % S, a = i % kAccStages;
-                if (!wait_bar(&bready[i], 0, p, misc)) break;
-                if (!wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc)) break;
-                if (i >= kAccStages && !wait_bar(&acce[a], static_cast<uint32_t>((i / kAccStages - 1) & 1), p, misc))
+            for (int i = 0; i < cnt && ok; ++i) {
+                const int s = i % S;
+                const int slot = i % p.KB;
+                const bool seg_start = i == 0 || kb == 0;
+                const int a = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) % NA);
+                const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
+                if (!kBlockScaled && !((known >> (16 + slot)) & 1u)) {
+                    const int j = slot;  // probe this slot and the next three
+                    known |= ptx::mbar_test4(&bready[j], 0, &bready[j + 1 < nslots ? j + 1 : j], 0,
+                                             &bready[j + 2 < nslots ? j + 2 : j], 0, &bready[j + 3 < nslots ? j + 3 : j], 0)
+                             << (16 + j);
+                    if (!((known >> (16 + slot)) & 1u)) {
+                        if (!wait_bar(&bready[slot], 0, p, misc)) break;
+                        known |= 1u << (16 + slot);
+                    }
+                }
+                if (!(i < S && ((known >> i) & 1u)) && !wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc))
                     break;
+                if ((seg_start || !kBlockScaled) && use > 0 &&
+                    !wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc))
+                    break;
+
                 ptx::tc_fence_after();
+#ifdef FP8BS_TRACE
+                if (i < 10) t_issue[i] = clock64();
+#endif
                 const uint32_t wa = ptx::smem_addr(sRing + s * kTileBytes);
-                const uint32_t xb = ptx::smem_addr(sB + i * C::kBBytes);
+                const uint32_t xb = ptx::smem_addr(sB + slot * C::kBBytes);
+                const uint32_t d = tmem + static_cast<uint32_t>(a * MPAD);
+                if constexpr (kBlockScaled) {
+                    const uint32_t sfa = tmem + C::kSfaCol + 4 * i;
+                    const uint32_t sfb = tmem + C::kSfbCol + 4 * slot;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    ptx::mma_f8f6f4(tmem + a * MPAD, ptx::smem_desc_sw128(wa + 32 * k),
-                                    ptx::smem_desc_sw128(xb + 32 * k), idesc, k > 0 ? 1u : 0u);
-                ptx::mma_commit(&empty[s]);  // frees the slot and publishes the accumulator
-                misc[kMiscCommitted + odd] = static_cast<uint32_t>(i + 1);
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_mxf8f6f4_bs(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k),
+                                             ptx::idesc_mxf8f6f4_e4m3_e8m0(128, MPAD, k, k), sfa, sfb,
+                                             (k > 0 || !seg_start) ? 1u : 0u);
+                } else {
+                    const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_f8f6f4(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k), idesc,
+                                        k > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&empty[s]);  // frees the ring slot
+                committed = i + 1;
+                const bool seg_end = ++kb == KB || i == cnt - 1;
+                // the stage's sum is complete: per unit (fp32), per segment (ue8m0).
+                // Its own barrier, not the ring's: that one can run a phase ahead
+                // before the epilogue looks; this one waits for the epilogue
+                if (!kBlockScaled || seg_end) ptx::mma_commit(&accfull[a]);
+                if (seg_end) {
+                    kb = 0;
+                    ++seg;
+                }
             }
+            misc[kMiscCommitted] = static_cast<uint32_t>(committed);
+#ifdef FP8BS_TRACE
+            FP8BS_STAMP_CLK(trec, kTpMmaLast);
+            for (int i = 0; i < 10 && i < committed; ++i) {
+                trec[2 * (kTpMmaUnit + i)] = 1;
+                trec[2 * (kTpMmaUnit + i) + 1] = static_cast<unsigned long long>(t_issue[i]);
+            }
+            if (committed > 0) {
+                trec[2 * kTpMmaFirst] = 1;
+                trec[2 * kTpMmaFirst + 1] = static_cast<unsigned long long>(t_issue[0]);
+            }
+#endif
         }
         __syncwarp();
-    } else {
-        if constexpr (SRC == kSrcLocal) {
-            // ---- 2. quantise this CTA's own units' groups --------------------------
-            // group g = i * M + m (unit i, token m); half-warp hw takes g = hw + 12 j.
-            // All loads are in flight first; the rolled loop then quantises
-            // raw[0] and shifts the rest down, so its body appears once.
-            const int ngc = cnt * p.M;
-            uint4 raw[C::kGroupsPerHw];
-#pragma unroll
-            for (int j = 0; j < C::kGroupsPerHw; ++j) {
-                const int g = hw + kQuantHalfWarps * j;
-                raw[j] = make_uint4(0, 0, 0, 0);
-                if (g < ngc) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(g), p.mdiv));
-                    const int m = g - i * p.M;
-                    raw[j] = __ldg(reinterpret_cast<const uint4*>(p.x + m * p.ldx + sKb[i] * kTile + l16 * 8));
-                }
-            }
-            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
-#pragma unroll 1
-            for (int j = 0; hw_first + kQuantHalfWarps * j < ngc; ++j) {  // warp-uniform
-                const int g = hw + kQuantHalfWarps * j;
-                const SliceQuant qs = quant_slice<KIND>(raw[0], sTab);
-                if (g < ngc) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(g), p.mdiv));
-                    const int m = g - i * p.M;
-                    if (u0 + i < KB) put_xq_out<KIND>(p, m, sKb[i], l16, qs);  // n-tile 0 publishes xq / xs
-                    put_slice<MPAD>(sB, sXs, bready, i, m, l16, qs.lo, qs.hi, qs.scale);
-                }
-#pragma unroll
-                for (int t = 0; t + 1 < C::kGroupsPerHw; ++t) raw[t] = raw[t + 1];
-            }
-        } else if constexpr (SRC == kSrcExchange) {
-            // ---- 2a. this CTA's share of all groups: quantise, publish ------------
-            // group g = kb * M + m; half-warp hw takes g0 + hw, g0 + hw + 12, ...
-            const uint32_t NG = static_cast<uint32_t>(p.M) * KB;
-            const uint32_t g0 = unit_begin(c, NG, G), g1 = unit_begin(c + 1, NG, G);
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (g0 + hw < g1) {
-                const uint32_t g = g0 + hw;
-                const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
-                raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
-            }
-            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
-#pragma unroll 1
-            for (uint32_t base = g0; base + hw_first < g1; base += kQuantHalfWarps) {  // warp-uniform
-                const uint32_t g = base + hw;
-                const bool valid = g < g1;
-                const uint32_t kb = div_m(g, p.mdiv), m = g - kb * static_cast<uint32_t>(p.M);
-                if (base != g0) {
-                    raw = make_uint4(0, 0, 0, 0);
-                    if (valid) raw = *reinterpret_cast<const uint4*>(p.x + m * p.ldx + kb * kTile + l16 * 8);
-                }
-                const SliceQuant qs = quant_slice<KIND>(raw, sTab);
-                if (valid) {  // no fence, no flag: each word carries the epoch
-                    st_pair(kb_codes(p, kb) + m * 32 + 2 * l16, tag(qs.lo, epoch), tag(qs.hi, epoch));
-                    if (l16 == 0)
-                        st_word(kb_scales(p, kb) + m, tag(KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale),
-                                                          epoch));
-                    put_xq_out<KIND>(p, m, kb, l16, qs);
-                }
-            }
-            // ---- 2b. the groups of this CTA's units into shared memory -------------
-            // chunk t = gi * 16 + l (group gi = i * M + m, 8 codes l): thread qt
-            // takes t = qt + 160 j, in rounds of kRound loads in flight; the stale
-            // ones are re-read together (one round trip per attempt, bounded)
-            // until both words carry the epoch.  Then the scales, the same way.
-            constexpr int kRound = 8;
-            const int ngc = cnt * p.M;
-            const int nch = ngc * 16;
-            bool ok = true;
-#pragma unroll 1
-            for (int base = 0; base < nch && ok; base += kQuantThreads * kRound) {
-                uint64_t w[kRound][2];
-#pragma unroll
-                for (int j = 0; j < kRound; ++j) {
-                    const int t = base + qt + kQuantThreads * j;
-                    w[j][0] = w[j][1] = tag(0, epoch);  // out of range: nothing to wait for
-                    if (t < nch) {
-                        const int gi = t >> 4, l = t & 15;
-                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                        const int m = gi - i * p.M;
-                        ld_pair(kb_codes(p, static_cast<uint32_t>(sKb[i])) + m * 32 + 2 * l, w[j][0], w[j][1]);
-                    }
-                }
-                const long long t0 = clock64();
-                while (true) {
-                    bool all = true;
-#pragma unroll
-                    for (int j = 0; j < kRound; ++j) all = all && tagged(w[j][0], epoch) && tagged(w[j][1], epoch);
-                    if (all) break;
-                    if (gave_up(t0, p, misc)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int j = 0; j < kRound; ++j) {
-                        const int t = base + qt + kQuantThreads * j;
-                        if (!(tagged(w[j][0], epoch) && tagged(w[j][1], epoch))) {
-                            const int gi = t >> 4, l = t & 15;
-                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                            const int m = gi - i * p.M;
-                            ld_pair(kb_codes(p, static_cast<uint32_t>(sKb[i])) + m * 32 + 2 * l, w[j][0], w[j][1]);
-                        }
-                    }
-                }
-                if (!ok) break;
-#pragma unroll
-                for (int j = 0; j < kRound; ++j) {
-                    const int t = base + qt + kQuantThreads * j;
-                    if (t < nch) {
-                        const int gi = t >> 4, l = t & 15;
-                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                        const int m = gi - i * p.M;
-                        uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
-                        *reinterpret_cast<uint2*>(row + (((l >> 1) ^ (m & 7)) << 4) + ((l & 1) << 3)) =
-                            make_uint2(static_cast<uint32_t>(w[j][0]), static_cast<uint32_t>(w[j][1]));
-                    }
-                }
-                ptx::fence_proxy_async_smem();
-#pragma unroll
-                for (int j = 0; j < kRound; ++j) {
-                    const int t = base + qt + kQuantThreads * j;
-                    if (t < nch) ptx::mbar_arrive(&bready[static_cast<int>(div_m(static_cast<uint32_t>(t >> 4), p.mdiv))]);
-                }
-            }
-            if (ok) {
-                uint64_t sw[C::kGroupsPerThread];
-#pragma unroll
-                for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                    const int gi = qt + kQuantThreads * j;
-                    sw[j] = tag(0, epoch);
-                    if (gi < ngc) {
-                        const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                        const int m = gi - i * p.M;
-                        sw[j] = ld_word(kb_scales(p, static_cast<uint32_t>(sKb[i])) + m);
-                    }
-                }
-                const long long t0 = clock64();
-                while (true) {
-                    bool all = true;
-#pragma unroll
-                    for (int j = 0; j < C::kGroupsPerThread; ++j) all = all && tagged(sw[j], epoch);
-                    if (all) break;
-                    if (gave_up(t0, p, misc)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                        const int gi = qt + kQuantThreads * j;
-                        if (!tagged(sw[j], epoch)) {
-                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                            const int m = gi - i * p.M;
-                            sw[j] = ld_word(kb_scales(p, static_cast<uint32_t>(sKb[i])) + m);
-                        }
-                    }
-                }
-                if (ok) {
-#pragma unroll
-                    for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                        const int gi = qt + kQuantThreads * j;
-                        if (gi < ngc) {
-                            const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                            const int m = gi - i * p.M;
-                            const uint32_t bits = static_cast<uint32_t>(sw[j]);
-                            sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(bits) : __uint_as_float(bits);
-                            ptx::mbar_arrive(&bready[i]);
-                        }
-                    }
-                }
-            }
-        } else {
-            // ---- 2. the caller's codes and scales of this CTA's units --------------
-            // group gi = i * M + m; thread qt takes gi = qt + 160 j: all copies in
-            // flight, then one wait.
-            const int ngc = cnt * p.M;
-            uint32_t sbits[C::kGroupsPerThread];
-#pragma unroll
-            for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                const int gi = qt + kQuantThreads * j;
-                sbits[j] = 0;
-                if (gi < ngc) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                    const int m = gi - i * p.M;
-                    const int kb = sKb[i];
-                    const uint8_t* src = p.xq_in + m * p.ldxq + kb * kTile;
-                    uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll 1
-                    for (int ch = 0; ch < 8; ++ch) ptx::cp_async16(row + ((ch ^ (m & 7)) << 4), src + ch * 16);
-                    sbits[j] = KIND == FP8BS_SCALE_UE8M0 ? static_cast<const uint8_t*>(p.xs_in)[m * p.KB + kb]
-                                                         : static_cast<const uint32_t*>(p.xs_in)[m * p.KB + kb];
-                }
-            }
-            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
-            ptx::cp_async_wait_all();
-#pragma unroll
-            for (int j = 0; j < C::kGroupsPerThread; ++j) {
-                const int gi = qt + kQuantThreads * j;
-                if (gi < ngc) {
-                    const int i = static_cast<int>(div_m(static_cast<uint32_t>(gi), p.mdiv));
-                    const int m = gi - i * p.M;
-                    sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? e8m0_to_float(sbits[j]) : __uint_as_float(sbits[j]);
-                    ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&bready[i]);
-                }
-            }
-        }
+    }
 
-        if (warp >= 4) {
-            // ---- 4./5. rescale-accumulate and output -------------------------------
-            const int q = warp & 3;
-            uint32_t hdr = 0;
-            if (lane == 0) hdr = wait_bar(hdr_bar, 0, p, misc) && misc[kMiscHdrOk] != 0;
-            const bool hdr_ok = __shfl_sync(0xFFFFFFFFu, hdr, 0) != 0;
-            float acc[MPAD];
+    if (warp >= 4) {
+        // ---- 4./5. accumulate and output -------------------------------------------
+        const int q = warp & 3;
+        const bool hdr_ok = warp_wait_bar(hdr_bar, 0, p, misc, lane) && misc[kMiscHdrOk] != 0;
+        float acc[MPAD];
+        uint32_t seg = 0;
+        int i = 0, seen = 0;  // seen: units whose MMAs are known to be complete
+        bool ok = true;
+#pragma unroll 1
+        while (i < cnt && ok) {
+            const uint32_t nt = nt0 + seg;
+            const int seg_end = static_cast<int>((nt + 1) * KB - u0);
+            const int ib = seg_end < cnt ? seg_end : cnt;
 #pragma unroll
             for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
-            uint32_t cur = nt0, kb = kb0;
-            // the CTAs holding the last units of this CTA's first and last tiles
-            // (only those two can be shared with other CTAs)
-            const uint32_t ntl = nt0 + (kb0 + static_cast<uint32_t>(cnt) - 1) / static_cast<uint32_t>(KB);
-            const uint32_t last0 = cta_of((nt0 + 1) * static_cast<uint32_t>(KB) - 1, p.T, G);
-            const uint32_t lastl = cta_of((ntl + 1) * static_cast<uint32_t>(KB) - 1, p.T, G);
-#pragma unroll 1
-            for (int i = 0; i < cnt; ++i) {
-                const int a = i % kAccStages;
-                uint32_t done = 0;
-                // the MMA completion (the slot's release: its phase cannot move on
-                // before every epilogue warp has freed this unit's TMEM stage), and
-                // the operand barrier that published sXs[i]
-                if (lane == 0)
-                    done = (wait_bar(&empty[i % S], static_cast<uint32_t>((i / S) & 1), p, misc) &&
-                            wait_bar(&bready[i], 0, p, misc)) ? 1u : 0u;
-                if (__shfl_sync(0xFFFFFFFFu, done, 0) == 0) break;
+            if constexpr (kBlockScaled) {
+                // the segment's sum is in TMEM stage seg % NA once its last MMA is done
+                const int a = static_cast<int>(seg % NA);
+                ok = warp_wait_bar(&accfull[a], static_cast<uint32_t>((seg / NA) & 1), p, misc, lane);
+                if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
-                uint32_t r[MPAD / 16][16];
-#pragma unroll
-                for (int h = 0; h < MPAD / 16; ++h) ptx::tmem_ld_32x32b_x16(taddr + 16 * h, r[h]);
-                ptx::tmem_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&acce[a]);  // this warp is done with the stage
-                const float sw = sWs[i];
 #pragma unroll
                 for (int h = 0; h < MPAD / 16; ++h) {
+                    uint32_t rr[16];
+                    ptx::tmem_ld_32x32b_x16(taddr + 16 * h, rr);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        acc[16 * h + m] = fmaf(__uint_as_float(r[h][m]), sXs[i * MPAD + 16 * h + m] * sw, acc[16 * h + m]);
+                    for (int m = 0; m < 16; ++m) acc[16 * h + m] = __uint_as_float(rr[m]);
                 }
-                if (++kb == KB || i == cnt - 1) {  // the tile ends here, or this CTA's range does
-                    // whole tile in this CTA -> 0; this CTA started inside the tile
-                    // -> 1 (publish); the tile goes on in later CTAs -> 2 (reduce;
-                    // always this CTA's last unit, so the weight ring is idle)
-                    const bool starts_here = cur != nt0 || kb0 == 0;
-                    const bool ends_here = kb == KB;
-                    const int role = starts_here ? (ends_here ? 0 : 2) : 1;
-                    if (hdr_ok && !flush_tile<MPAD, C::kRingBytes / 16, TAGGED>(p, cur, acc, c, cur == nt0 ? last0 : lastl,
-                                                                                 role, q, lane, epoch, misc,
-                                                                                 reinterpret_cast<float*>(sRing)))
-                        break;
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&acce[a]);
+                i = ib;
+            } else {
+#pragma unroll 1
+                for (; i < ib; ++i) {
+                    const int a = i % NA;
+                    if (i >= seen) {
+                        // units complete in order: one probe of the unit three
+                        // on may cover four; else wait for this one
+                        const int j = i + 3 < cnt ? i + 3 : cnt - 1;
+                        uint32_t got = 0;
+                        if (lane == 0) got = ptx::mbar_test(&accfull[j % NA], static_cast<uint32_t>((j / NA) & 1)) ? 1u : 0u;
+                        if (__shfl_sync(0xFFFFFFFFu, got, 0) != 0) {
+                            seen = j + 1;
+                        } else {
+                            ok = warp_wait_bar(&accfull[a], static_cast<uint32_t>((i / NA) & 1), p, misc, lane);
+                            if (!ok) break;
+                            seen = i + 1;
+                        }
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
+                    const float sw = sWs[i];
+                    const uint32_t* xs = sXs + (i % p.KB) * MPAD;
 #pragma unroll
-                    for (int m = 0; m < MPAD; ++m) acc[m] = 0.0f;
-                    ++cur;
-                    kb = 0;
+                    for (int h = 0; h < MPAD / 16; ++h) {
+                        uint32_t rr[16];
+                        ptx::tmem_ld_32x32b_x16(taddr + 16 * h, rr);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            acc[16 * h + m] =
+                                fmaf(__uint_as_float(rr[m]), __uint_as_float(xs[16 * h + m]) * sw, acc[16 * h + m]);
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&acce[a]);
+                    if (i < 10 && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiUnit + i);
                 }
+                if (!ok) break;
             }
+            if (ib == cnt && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiLast);
+            // the tile's contributors; an owner's segment is always the CTA's last
+            const uint32_t c0 = cta_of(nt * KB, p.T, G), c1 = cta_of(nt * KB + KB - 1, p.T, G);
+            if (hdr_ok)
+                ok = flush_segment<MPAD>(p, nt, acc, c, c0, c1, G, q, lane, epoch, misc,
+                                         reinterpret_cast<float*>(sRing) + q * C::kStageFloats);
+            if (tid == 128) FP8BS_STAMP_CLK(trec, c == c1 && c0 != c1 ? kTpPublish : kTpReduceEnd);
+            ++seg;
         }
     }
 
     // ---- teardown -------------------------------------------------------------
     ptx::tc_fence_before();
     __syncthreads();
+    if (tid == 0) FP8BS_STAMP(trec, kTpTeardown);
     if (misc[kMiscAbort] != 0 && tid == 0) {
         // drain this CTA's own copies and MMAs before its shared memory and
         // TMEM go away (bounded as well)
@@ -801,12 +819,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
             const int uses = (issued - 1 - s) / S + 1;
             drain_bar(&full[s], static_cast<uint32_t>((uses - 1) & 1), p.timeout);
         }
-        for (int odd = 0; odd < 2; ++odd) {
-            const int committed = static_cast<int>(misc[kMiscCommitted + odd]);
-            if (committed > 0) {  // the issuer's last commit covers all of its MMAs
-                const int j = committed - 1;
-                drain_bar(&empty[j % S], static_cast<uint32_t>((j / S) & 1), p.timeout);
-            }
+        const int committed = static_cast<int>(misc[kMiscCommitted]);
+        if (committed > 0) {  // the issuer's last commit covers all of its MMAs
+            const int j = committed - 1;
+            drain_bar(&empty[j % S], static_cast<uint32_t>((j / S) & 1), p.timeout);
         }
     }
     __syncthreads();
@@ -817,22 +833,31 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, SRC>::kCtasPerSm)
     // every thread has read the old epoch: move this index class on to it
     if (warp == 2)
         for (uint32_t j = c + lane * G; j < static_cast<uint32_t>(kMaxCtas); j += 32 * G) p.gen[j] = epoch;
+#ifdef FP8BS_TRACE
+    if (warp == 2) {
+        if (lane == 0) FP8BS_STAMP(trec, kTpExit);
+        __syncwarp();
+        if (c < static_cast<uint32_t>(kTraceCtas))
+            for (int v = lane; v < 2 * kTpCount; v += 32)
+                g_trace[((epoch % kTraceCalls) * kTraceCtas + c) * (2 * kTracePoints) + v] = trec[v];
+    }
+#endif
 }
 
-template <int MPAD, int KIND, int SRC, bool TAGGED>
+template <int MPAD, int KIND, int SRC>
 cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
-    using C = Cfg<MPAD, SRC>;
-    auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC, TAGGED>;
+    using C = Cfg<MPAD, KIND>;
+    auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC>;
     // Opt in to the dynamic shared memory once per device (not a stream
     // operation, so it is harmless during graph capture too).
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = 1;
+        if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -847,12 +872,12 @@ cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int MPAD, int KIND, int SRC, bool TAGGED>
+template <int MPAD, int KIND, int SRC>
 cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
     // At most one CTA per SM with at most kUnits units each: weights with more
     // units than that go in several launches of whole n-tiles.
     const int KB = a.K / kTile, NT = a.N / kTile;
-    const int cap_units = a.sm_count * Cfg<MPAD, SRC>::kUnits;
+    const int cap_units = a.sm_count * Cfg<MPAD, KIND>::kUnits;
     const int chunk_nt = cap_units / KB;  // >= 1 (checked by the caller)
     const size_t scale_bytes = a.kind == FP8BS_SCALE_UE8M0 ? 1 : 4;
     for (int nt_base = 0; nt_base < NT; nt_base += chunk_nt) {
@@ -865,7 +890,7 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
         p.xs_out = nt_base == 0 ? a.xs_out : nullptr;
         p.pdl = nt_base == 0 ? a.pdl : 1;  // later chunks follow our own launch, which never writes packed
         const int grid = static_cast<int>(p.T) < a.sm_count ? static_cast<int>(p.T) : a.sm_count;
-        const cudaError_t e = launch_impl<MPAD, KIND, SRC, TAGGED>(p, grid, stream);
+        const cudaError_t e = launch_impl<MPAD, KIND, SRC>(p, grid, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -874,21 +899,18 @@ cudaError_t launch_chunks(Params p, const FusedArgs& a, cudaStream_t stream) {
 template <int KIND>
 cudaError_t launch_kind(const Params& p, const FusedArgs& a, cudaStream_t stream) {
     if (a.xq_in) {
-        if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcInput, true>(p, a, stream);
-        if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput, false>(p, a, stream);
-        if (a.M <= 32) return launch_chunks<32, KIND, kSrcInput, false>(p, a, stream);
-        return launch_chunks<64, KIND, kSrcInput, false>(p, a, stream);
+        if (a.M <= 16) return launch_chunks<16, KIND, kSrcInput>(p, a, stream);
+        if (a.M <= 32) return launch_chunks<32, KIND, kSrcInput>(p, a, stream);
+        return launch_chunks<64, KIND, kSrcInput>(p, a, stream);
     }
-    if (a.M <= kLocalMaxM) return launch_chunks<16, KIND, kSrcLocal, true>(p, a, stream);
-    if (a.M <= kTaggedMaxM) return launch_chunks<16, KIND, kSrcExchange, true>(p, a, stream);
-    if (a.M <= 16) return launch_chunks<16, KIND, kSrcExchange, false>(p, a, stream);
-    if (a.M <= 32) return launch_chunks<32, KIND, kSrcExchange, false>(p, a, stream);
-    return launch_chunks<64, KIND, kSrcExchange, false>(p, a, stream);
+    if (a.M <= 16) return launch_chunks<16, KIND, kSrcQuant>(p, a, stream);
+    return launch_chunks<32, KIND, kSrcQuant>(p, a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
+    if (!a.xq_in && a.M > kFusedMaxM) return cudaErrorInvalidValue;  // the API routes these through two launches
     Params p;
     p.x = a.x;
     p.ldx = a.ldx;
@@ -902,9 +924,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.ldy = a.ldy;
     p.err = reinterpret_cast<uint32_t*>(a.workspace);
     p.gen = reinterpret_cast<uint32_t*>(a.workspace + ws_gen_offset());
-    p.pflag = reinterpret_cast<uint32_t*>(a.workspace + ws_pflag_offset());
     p.slots = reinterpret_cast<uint64_t*>(a.workspace + ws_partials_offset());
-    p.act = a.workspace + ws_act_offset(a.sm_count);
     p.xq_in = a.xq_in;
     p.ldxq = a.ldxq;
     p.xs_in = a.xs_in;
@@ -912,6 +932,17 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream) {
     p.pdl = a.pdl;
     if (a.kind == FP8BS_SCALE_UE8M0) return launch_kind<FP8BS_SCALE_UE8M0>(p, a, stream);
     return launch_kind<FP8BS_SCALE_F32>(p, a, stream);
+}
+
+cudaError_t trace_copy(void* host_dst, size_t bytes) {
+#ifdef FP8BS_TRACE
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return cudaMemcpyFromSymbol(host_dst, g_trace, bytes);
+#else
+    (void)host_dst;
+    (void)bytes;
+    return cudaErrorNotSupported;
+#endif
 }
 
 bool fused_shape_supported(int64_t N, int64_t K, int sm_count) {

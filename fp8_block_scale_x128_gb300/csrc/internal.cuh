@@ -33,42 +33,42 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
     return kHeaderBytes + static_cast<size_t>(N / kTile) * static_cast<size_t>(K / kTile) * kTileBytes;
 }
 
-// Workspace layout (bytes).  The CTAs of one fused launch exchange two kinds
-// of data through it: the quantised activations (each 1x128 group published
-// once, by one CTA) and the split-K partials.  The activations, and the
-// partials of a tile with few of them, travel as 64-bit words, 32 data bits
-// and the call's 32-bit epoch, so a reader sees either an older word or the
-// new one and needs no flag.  The partials of other tiles are plain fp32,
-// followed by a flag per epilogue warp set to the epoch.  Words and flags
-// left by earlier calls carry older epochs, so nothing is cleared between
-// calls.  Every region sits at a place that depends on sm_count only, never
-// on N or K, so a workspace serves calls of any shape without a word of one
-// call ever being taken for one of another.
+// Workspace layout (bytes).  The CTAs of one fused launch exchange their
+// split-K partials through it: each partial value travels as a 64-bit word,
+// 32 data bits and the call's 32-bit epoch, so a reader sees either an older
+// word or the new one and needs no flag.  Words left by earlier calls carry
+// older epochs, so nothing is cleared between calls.  Every region sits at a
+// place that depends on sm_count only, never on N or K, so a workspace serves
+// calls of any shape without a word of one call ever being taken for one of
+// another.
 //   [0, 256)                  device error word
 //   [256, +4 KB)              epoch words, one per possible CTA index
-//   [4352, +16 KB)            partial flags, one per (CTA index, epilogue warp)
-//   then sm_count x 32 KB     split-K partial slots: [32 columns][128 rows] of
-//                             tagged words, or [64 columns][128 rows] of fp32
-//   then K/128 x 16896 B      one record per K block of the activations:
-//                             64 scale words, 64 rows x 32 words of 4 codes
+//   then sm_count x 2 x 64 KB split-K partial slots: per CTA index one for the
+//                             first and one for the last n-tile of its range,
+//                             each [64 columns][128 rows] of tagged words
+//   then 64 x K + 64 x K/128 x 4  codes and scales of the routed two-launch
+//                             path (33 to 64 tokens) when the caller does not
+//                             ask for them
 constexpr size_t kWsErrorBytes = 256;
 constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
 constexpr size_t kWsGenBytes = kMaxCtas * sizeof(uint32_t);
-constexpr size_t kWsPflagBytes = kMaxCtas * 4 * sizeof(uint32_t);
-constexpr size_t kSlotBytes = 32 * 128 * sizeof(uint64_t);
-constexpr size_t kKbRecScales = 0;                       // within a K-block record
-constexpr size_t kKbRecCodes = 64 * sizeof(uint64_t);
-constexpr size_t kKbRecBytes = kKbRecCodes + 64 * 32 * sizeof(uint64_t);
+constexpr size_t kSlotWords = 64 * 128;
+constexpr size_t kSlotBytes = kSlotWords * sizeof(uint64_t);
+constexpr int kSlotsPerCta = 2;
 
 __host__ __device__ constexpr size_t ws_gen_offset() { return kWsErrorBytes; }
-__host__ __device__ constexpr size_t ws_pflag_offset() { return kWsErrorBytes + kWsGenBytes; }
-__host__ __device__ constexpr size_t ws_partials_offset() { return ws_pflag_offset() + kWsPflagBytes; }
+__host__ __device__ constexpr size_t ws_partials_offset() { return kWsErrorBytes + kWsGenBytes; }
 __host__ __device__ constexpr size_t ws_act_offset(int sm_count) {
-    return ws_partials_offset() + static_cast<size_t>(sm_count) * kSlotBytes;
+    return ws_partials_offset() + static_cast<size_t>(sm_count) * kSlotsPerCta * kSlotBytes;
 }
 __host__ __device__ constexpr size_t ws_total_bytes(int sm_count, int64_t K) {
-    return ws_act_offset(sm_count) + static_cast<size_t>(K / kTile) * kKbRecBytes;
+    return ws_act_offset(sm_count) + static_cast<size_t>(FP8BS_MAX_M) * static_cast<size_t>(K) +
+           static_cast<size_t>(FP8BS_MAX_M) * static_cast<size_t>(K / kTile) * sizeof(float);
 }
+
+// Largest token count the fused kernel quantises itself; fp8bs_gemm_fused
+// runs larger calls as the quant, then the GEMM on its codes.
+constexpr int kFusedMaxM = 32;
 
 // Units of work (128x128 weight tiles) one CTA of the fused kernel owns at most.
 constexpr int kMaxUnitsM16 = 12;
@@ -151,22 +151,6 @@ __device__ __forceinline__ void fill_scale_table(float2* tab, int t, int nthread
     }
 }
 
-// True when the e4m3 code of a (an fp32 product within 2 ulps of the real
-// quotient t = x / scale) may differ from the code of q = RN32(t):
-//  * |a| in [2^-6, 512): e4m3 keeps 3 mantissa bits, so every rounding
-//    boundary (the midpoint of two neighbouring codes) has low 20 mantissa
-//    bits 0x80000.  q lies within 3 bit-steps of a inside a binade (5 across
-//    a binade edge, where no boundary is near), so an a more than 8 steps
-//    away from that pattern rounds like q;
-//  * 0 < |a| < 2^-6: the e4m3 subnormal range, where the boundary pattern
-//    moves with the exponent; rare, so such values take the exact path;
-//  * a = +-0 means x = +-0, whose code is exact.
-__device__ __forceinline__ bool e4m3_near_boundary(float a) {
-    const uint32_t mag = __float_as_uint(a) & 0x7FFFFFFFu;
-    const uint32_t low = (mag & 0xFFFFFu) - 0x80000u + 8u;  // in [0, 16] near the pattern
-    return mag != 0 && (mag < 0x3C800000u || low <= 16u);
-}
-
 // Result of quantising one 16-byte slice (8 values) of a 1x128 group.
 struct SliceQuant {
     uint32_t lo, hi;  // 8 codes, little-endian (the slice's first value in bits 0-7 of lo)
@@ -178,12 +162,15 @@ struct SliceQuant {
 // values per lane (lane l of the half-warp holds k = 8l .. 8l+7).  All 32
 // lanes of the warp must call it (each half-warp holds its own group).
 //
-// The codes are those of RN32(x / scale), found exactly without a division in
-// the common case: a = x * r with r = RN32(1 / scale) lies within 2 ulps of
-// the real quotient, and cvt(a) is the code of the correctly rounded quotient
-// unless a sits within a few bit-steps of an e4m3 rounding boundary
-// (e4m3_near_boundary, about 2^-16 of all values), where the IEEE quotient is
-// computed instead.  ue8m0 scales are powers of two, so there x * (1 / scale)
+// The codes are those of RN32(x / scale), computed without a division:
+// from the correctly rounded reciprocal r = RN32(1 / scale), q0 = RN32(x r),
+// the remainder x - q0 scale (an fma, exact), and q = RN32(q0 + remainder r)
+// (an fma) is the correctly rounded quotient -- the division step of P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990, which needs the reciprocal
+// correctly rounded and no intermediate to over- or underflow.  Groups whose
+// amax is below 2^-60 (their remainders could be subnormal) take the IEEE
+// division instead.  ue8m0 scales are powers of two, so there x * (1 / scale)
 // is the quotient itself.
 template <int KIND>
 __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __restrict__ tab) {
@@ -227,24 +214,23 @@ __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __res
     } else {
         out.scale = s;
     }
-    float a[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) a[j] = v[j] * recip;
-    bool exact = KIND == FP8BS_SCALE_UE8M0;
-    if (!exact) {
-        bool near = !(amax >= 0x1p-100f);  // tiny groups: 1 / scale may overflow
-#pragma unroll
-        for (int j = 0; j < 8; ++j) near |= e4m3_near_boundary(a[j]);
-        exact = !near;
-    }
-    if (exact) {
-        out.lo = e4m3x2(a[0], a[1]) | (e4m3x2(a[2], a[3]) << 16);
-        out.hi = e4m3x2(a[4], a[5]) | (e4m3x2(a[6], a[7]) << 16);
-    } else {
+    if (KIND == FP8BS_SCALE_F32 && !(amax >= 0x1p-60f)) {
+        // tiny groups: the IEEE quotients throughout
         const uint2 c = e4m3_codes8_divide(raw, s);
         out.lo = c.x;
         out.hi = c.y;
+        return out;
     }
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a[j] = v[j] * recip;
+        // the correction gives +0 for x = -0 (0 + -0 rounds to +0): the
+        // quotient keeps the sign of x, which copysign restores
+        if (KIND == FP8BS_SCALE_F32) a[j] = copysignf(fmaf(fmaf(-a[j], s, v[j]), recip, a[j]), v[j]);
+    }
+    out.lo = e4m3x2(a[0], a[1]) | (e4m3x2(a[2], a[3]) << 16);
+    out.hi = e4m3x2(a[4], a[5]) | (e4m3x2(a[6], a[7]) << 16);
     return out;
 }
 

@@ -53,6 +53,27 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// Four probes in one go: bit j of the result is set once barrier j's phase
+// with parity pj has completed.  A probe takes about 180 cycles to answer;
+// issued together the four answer in about the time of one.
+__device__ __forceinline__ uint32_t mbar_test4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                               uint32_t p2, uint64_t* b3, uint32_t p3) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3;\n\t.reg .b32 t0, t1, t2, t3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "selp.u32 t0, 1, 0, q0;\n\tselp.u32 t1, 2, 0, q1;\n\tselp.u32 t2, 4, 0, q2;\n\tselp.u32 t3, 8, 0, q3;\n\t"
+        "or.b32 t0, t0, t1;\n\tor.b32 t2, t2, t3;\n\tor.b32 %0, t0, t2;\n\t}"
+        : "=r"(r)
+        : "r"(smem_addr(b0)), "r"(p0), "r"(smem_addr(b1)), "r"(p1), "r"(smem_addr(b2)), "r"(p2), "r"(smem_addr(b3)),
+          "r"(p3)
+        : "memory");
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Bulk async copy global -> shared, completion counted on an mbarrier.
 // dst and src 16-byte aligned; bytes a multiple of 16.
@@ -116,6 +137,15 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 // Bring the 128-byte line holding p into L2 (no data returned, no ordering).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 16-byte global load that the compiler keeps where it is written: it is
+// neither re-issued later (to free registers) nor moved past other volatile
+// instructions, so a batch of these is in flight together.
+__device__ __forceinline__ uint4 ld_global_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
 }
 
 // Wait until every cp.async this thread issued has landed in shared memory.
@@ -218,6 +248,40 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;
     return d;
+}
+
+// D[tmem] (+)= (A[smem] * sfa) * (B[smem] * sfb)^T, e4m3 x e4m3 -> fp32, with
+// one e8m0 scale factor per 32 K values of each row of A and of B read from
+// TMEM (kind::mxf8f6f4.block_scale.scale_vec::1X).  Row r of A takes its
+// factor from TMEM lane r, column sfa.col + r/32; row n of B from lane n % 32
+// of the quadrant the D row lies in, column sfb.col + n/32; the byte within
+// the 32-bit cell is the instruction descriptor's scale-factor id.
+__device__ __forceinline__ void mma_mxf8f6f4_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// One 32-bit TMEM cell per thread: thread i of the warp writes lane
+// taddr.lane + i, column taddr.col (the warp's own lane quadrant).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: B's scale-factor
+// id in bits 4-5, A and B e4m3 (bits 7-9, 10-12 = 0), both K-major, N >> 3 in
+// bits 17-22, scale-factor type e8m0 (bit 23 = 1), M >> 4 in bits 24-28, A's
+// scale-factor id in bits 29-30.
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3_e8m0(uint32_t m, uint32_t n, uint32_t sfa_id,
+                                                               uint32_t sfb_id) {
+    return (sfb_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) | (sfa_id << 29);
 }
 
 // Instruction descriptor, kind::f8f6f4, dense: D fp32 (bits 4-5 = 1), A and B

@@ -325,7 +325,7 @@ int fp8bs_moe_w8a16(const uint16_t* x, int64_t M, int64_t H, const int32_t* topk
 #define FP8BS_STATIC_MAX_SMS 160  /* CTAs it uses at most (grid cap)        */
 
 /* fp8bs_gemm_fused without a workspace argument: the scratch lives in one
- * fixed device array inside this library (7,426,304 bytes per device,
+ * fixed device array inside this library (22,057,216 bytes per device,
  * sized for FP8BS_STATIC_MAX_SMS CTAs and K up to FP8BS_STATIC_MAX_K), so the
  * call allocates no device memory, ever.  It is meant for callers that cannot
  * allocate or own device memory: an operator plugged into a runtime whose
@@ -342,13 +342,14 @@ int fp8bs_moe_w8a16(const uint16_t* x, int64_t M, int64_t H, const int32_t* topk
  *   status_out: optional (NULL to skip) device uint32 that receives, in stream
  *   order after the kernel, the scratch's error word: 0, or the negated
  *   status (FP8BS_ERR_TIMEOUT, FP8BS_ERR_SCALE_KIND) of the first device-side
- *   failure of any call on this device.  The word is sticky: this entry point
- *   cannot re-initialise the shared scratch, so after a timeout its epoch
- *   words may disagree and later calls may time out too.
+ *   failure since the last call that passed a status_out; the word is then
+ *   cleared in stream order.  After a timeout the scratch's epoch words may
+ *   disagree, and this entry point cannot re-initialise them: later calls may
+ *   time out too.
  * Set-up: the first call on each device (with that device current) looks up
  * the array's address with cudaGetSymbolAddress, zeroes it on `stream` and
- * waits for that; make the first call before any stream
- * capture.
+ * waits for that.  Make that first call outside stream capture: on a
+ * capturing stream it returns FP8BS_ERR_ARG and enqueues nothing.
  * Sharing: every call on one device uses the same array, so two calls that
  * can overlap (different streams, different host threads without ordering)
  * race and may time out or return wrong results.  Calls in order on one
@@ -357,6 +358,28 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
                             size_t packed_bytes, int64_t N, int64_t K, int scale_kind,
                             uint16_t* y, int64_t ldy, uint8_t* xq_out, void* xs_out,
                             uint32_t* status_out, unsigned flags, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Timeline tracing (profiling aid; no counterpart on the pages)             */
+/* ------------------------------------------------------------------------ */
+
+#define FP8BS_TRACE_CALLS 256  /* calls kept, by workspace epoch modulo 256  */
+#define FP8BS_TRACE_CTAS 160   /* CTAs kept per call                         */
+#define FP8BS_TRACE_POINTS 48  /* phase stamps per CTA                       */
+
+/* Copy the per-phase timeline of the fused GEMM's most recent calls to host
+ * memory.  Only a library built with tracing records one (native_build's
+ * trace=True, which compiles the kernels with FP8BS_TRACE; every CTA then
+ * stamps its phase boundaries with %globaltimer and clock64); the plain
+ * library keeps no timeline, returns FP8BS_ERR_ARG and copies nothing.
+ *   host_dst: host buffer of `bytes` bytes; receives the first `bytes` bytes of
+ *             uint64 [FP8BS_TRACE_CALLS][FP8BS_TRACE_CTAS][FP8BS_TRACE_POINTS][2]
+ *             (globaltimer ns, clock64 cycles), call slot = the call's
+ *             workspace epoch modulo FP8BS_TRACE_CALLS, point order as in the
+ *             library's csrc/trace.cuh; a stamp that was not taken is 0.
+ * Synchronises with the device (a blocking copy).  Errors: FP8BS_ERR_ARG (no
+ * tracing in this build, or a null buffer), FP8BS_ERR_CUDA. */
+int fp8bs_trace_read(void* host_dst, size_t bytes);
 
 #ifdef __cplusplus
 }

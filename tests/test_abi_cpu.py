@@ -52,7 +52,9 @@ def test_packed_weight_bytes(L):
 
 def test_workspace_bytes_for_explicit_sm_count(L):
     def expect(K, sm):
-        return 256 + 4096 + 16384 + sm * 32 * 128 * 8 + (K // 128) * (64 * 8 + 64 * 32 * 8)
+        # error word, epoch words, two 64 x 128 tagged-word partial slots per
+        # CTA index, then the codes and fp32 scales of up to 64 rows
+        return 256 + 4096 + sm * 2 * 64 * 128 * 8 + 64 * K + 64 * (K // 128) * 4
     assert fb.fp8bs_workspace_bytes(5120, 4096, 152) == expect(4096, 152)
     assert fb.fp8bs_workspace_bytes(128, 128, 152) == expect(128, 152)
     # independent of N

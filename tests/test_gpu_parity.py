@@ -479,3 +479,86 @@ def test_fused_host_errors_raise(dev, oracle_mod):
 def test_binding_uses_native_library(dev):
     maps = open(f"/proc/{os.getpid()}/maps").read()
     assert "libfp8bs.so" in maps
+
+
+# ---------------------------------------------------------------------------
+# special 1x128 groups through every fused variant
+# ---------------------------------------------------------------------------
+
+def _special_rows(K: int) -> list:
+    """fp32 rows (later rounded to bf16) of the groups the quant treats specially,
+    whole rows first, then single special groups inside otherwise normal rows.
+    Returns a list of (name, fp32 row, check_row): check_row is False for the
+    row whose every scale is an fp32 subnormal, where the fp32 product
+    xs * ws of the rescale ("[AMD] Small-M FP8 block-scale GEMM with fused
+    activation quant for gfx950 (Qwen3.5)", "Modifications": the scales are
+    applied in fp32) underflows while the oracle's fp64 does not; that row is
+    covered by the whole-output criterion and the bit-exact codes."""
+    normal = lambda s: synth.bf16_bits_to_f32(synth.x_bf16(1, K, seed=s)[0])
+    rows = []
+    z = np.zeros(K, np.float32)
+    z[1::2] = -0.0
+    rows.append(("zero row with -0", z, True))
+    rows.append(("all-equal row", np.full(K, 3.0, np.float32), True))
+    rows.append(("row x 1e-30", normal(11) * np.float32(1e-30), True))
+    rows.append(("row x 1e30", normal(12) * np.float32(1e30), True))
+    sub = np.full(K, np.float32(2.0 ** -130), np.float32)
+    sub[5::7] = -np.float32(2.0 ** -133)
+    rows.append(("bf16 subnormal row", sub, False))
+    tie = np.tile(np.float32([448.0, 17.0, -19.0, 21.0, -0.0, 1.0, 3.0, -448.0]), K // 8)
+    rows.append(("exact e4m3 ties at scale 1", tie, True))
+    r = normal(13)
+    r[128:256] = -0.0                           # one zero group
+    r[256:384] = 3.0                            # one all-equal group
+    rows.append(("normal row, zero and all-equal groups", r, True))
+    r = normal(14)
+    r[0] = 3.0e38                               # one huge value in group 0
+    r[1:128] = 1.0
+    r[384] = -3.0e38                            # and a negative one in group 3
+    rows.append(("normal row, +-3e38 groups", r, True))
+    r = normal(15)
+    r[128:256] = np.float32(2.0 ** -130)        # one bf16-subnormal group
+    r[129] = -np.float32(2.0 ** -133)
+    r[256:384] = 448.0                          # one group at scale 1 with a tie
+    r[257] = 17.0
+    rows.append(("normal row, subnormal and tie groups", r, True))
+    return rows
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+@pytest.mark.parametrize("M", [3, 9, 17, 33, 48])
+def test_fused_special_groups(dev, oracle_mod, kind, M):
+    # M = 3: every CTA quantises its own groups; 9 and 17: each group quantised
+    # once and exchanged (tagged / flagged split-K partials); 33: the 64-token
+    # tile; 48: the quant then the GEMM on its codes.  Every special row goes
+    # through each variant (in chunks of M rows, the rest normal rows).  Quant
+    # bytes and scales bit-exact; y within the tolerance as a whole and row by
+    # row.
+    N, K = 5120, 4096
+    specials = _special_rows(K)
+    wq, ws = H.weight(oracle_mod, N, K, kind, 901)
+    packed = fb.fp8bs_prepack_weight(to_dev(wq, dev), to_dev(ws, dev), kind)
+    wsp = fb.new_workspace(N, K, dev)
+    for start in range(0, len(specials), M):
+        chunk = specials[start:start + M]
+        v = synth.bf16_bits_to_f32(synth.x_bf16(M, K, seed=900 + M + start))
+        names, check = ["normal"] * M, [True] * M
+        for i, (name, row, ok) in enumerate(chunk):
+            v[i], names[i], check[i] = row, name, ok
+        x = synth.f32_to_bf16_bits(v)
+        y_ref, xq_ref, xs_ref = oracle_mod.linear(x, wq, ws, kind, nthreads=H.threads())
+        assert np.all(np.isfinite(H.bf16_to_f32(y_ref)))
+        xq = torch.zeros((M, K), dtype=torch.uint8, device=dev)
+        xs = torch.zeros((M, K // 128), dtype=torch.uint8 if kind == UE8 else torch.float32, device=dev)
+        yd = fb.fp8bs_gemm_fused(x_dev(x, dev), packed, N, K, kind, workspace=wsp, xq_out=xq, xs_out=xs)
+        assert fb.fp8bs_check_error(wsp) == 0
+        got_q, got_s = xq.cpu().numpy(), xs.cpu().numpy()
+        for i in range(M):
+            assert np.array_equal(got_q[i], xq_ref[i]), f"codes of row {i} ({names[i]})"
+            assert np.array_equal(got_s[i].view(np.uint8), xs_ref[i].view(np.uint8)), \
+                f"scales of row {i} ({names[i]})"
+        y = H.torch_u16_to_np(yd)
+        H.check_y(y, y_ref, f"special groups M={M} kind={kind} chunk {start}")
+        for i in range(M):
+            if check[i]:
+                H.check_y(y[i:i + 1], y_ref[i:i + 1], f"row {i} ({names[i]}) M={M} kind={kind}")
