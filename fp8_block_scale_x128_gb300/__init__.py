@@ -391,7 +391,7 @@ def fp8bs_gemm_fused_static(x: torch.Tensor, packed: torch.Tensor, N: int, K: in
     return y
 
 
-FP8BS_TRACE_CALLS, FP8BS_TRACE_CTAS, FP8BS_TRACE_POINTS = 256, 160, 48
+FP8BS_TRACE_CALLS, FP8BS_TRACE_CTAS, FP8BS_TRACE_POINTS = 256, 160, 64
 
 
 def fp8bs_trace_read():

@@ -77,7 +77,7 @@ cudaError_t launch_fused_routed(FusedArgs a, cudaStream_t stream) {
     uint8_t* act = a.workspace + ws_act_offset(a.sm_count);
     uint8_t* xq = a.xq_out ? a.xq_out : act;
     void* xs = a.xs_out ? a.xs_out : static_cast<void*>(act + static_cast<size_t>(FP8BS_MAX_M) * a.K);
-    const cudaError_t e = launch_quant(a.x, a.M, a.K, a.ldx, a.kind, xq, xs, stream);
+    const cudaError_t e = launch_quant(a.x, a.M, a.K, a.ldx, a.kind, xq, xs, stream, a.pdl != 0);
     if (e != cudaSuccess) return e;
     a.xq_in = xq;
     a.ldxq = a.K;

@@ -74,6 +74,8 @@ constexpr int kThreads = 256;
 constexpr int kQuantHalfWarps = 14;  // warps 0 and 2-7
 constexpr int kQuantThreads = 16 * kQuantHalfWarps;
 constexpr int kQuantDepth = 4;       // groups per half-warp with their x loads in flight
+constexpr long long kSpinCycles = 4000;         // a wait probes without pause this long (~2 us) ...
+constexpr unsigned kBackoffNs = 128;            // ... then sleeps this long between probes
 
 // Where the activation codes come from.
 enum : int {
@@ -188,16 +190,23 @@ __device__ __noinline__ void raise_timeout(uint32_t* err, volatile uint32_t* mis
 }
 
 // Bounded wait for an mbarrier phase by one thread: false on expiry (recorded)
-// or once the CTA has aborted.
+// or once the CTA has aborted.  It probes without pause for kSpinCycles, then
+// sleeps kBackoffNs between probes: a wait that long is a CTA waiting for its
+// turn (the issuer and the epilogue of the next call's CTA wait through this
+// call), and a spinning warp takes issue slots from the warps that work on
+// the same SM (the activation quantisation was measured 2-3x slower with the
+// waiters of the co-resident CTA spinning).
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, volatile uint32_t* misc) {
     if (ptx::mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (!ptx::mbar_test(bar, parity)) {
         if (misc[kMiscAbort] != 0) return false;
-        if (clock64() - t0 > p.timeout) {
+        const long long dt = clock64() - t0;
+        if (dt > p.timeout) {
             raise_timeout(p.err, misc);
             return false;
         }
+        if (dt > kSpinCycles) __nanosleep(kBackoffNs);
     }
     return true;
 }
@@ -436,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
             ptx::bulk_prefetch_l2(p.tiles + static_cast<size_t>(u0 + pre) * kTileBytes,
                                   static_cast<uint32_t>(cnt - pre) * kTileBytes);
     }
+
     if (warp == 1) {
         ptx::tmem_alloc(const_cast<uint32_t*>(&misc[kMiscTmem]), C::kTmemCols);
         ptx::tmem_relinquish();
@@ -478,6 +488,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
     const int l16 = qt & 15;
     const int hw_first = hw & ~1;  // the warp's first half-warp
     uint32_t epoch = 0;
+    // ring refills (warp 0, lane 0): units S.. go into the slots their
+    // predecessors free.  Between quantisation rounds the ring thread issues
+    // those whose slots are already free, without waiting; after its share of
+    // the quantisation it takes the rest in order, waiting for each slot.
+    int refilled = S;
+    const auto refill = [&](int i) {
+        ptx::mbar_arrive_expect_tx(&full[i % S], kTileBytes);
+        ptx::bulk_g2s(sRing + (i % S) * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
+                      &full[i % S], ptx::policy_evict_first());
+        misc[kMiscIssued] = static_cast<uint32_t>(i + 1);
+        if (i - S < 8) FP8BS_STAMP_CLK(trec, kTpRefill + i - S);
+    };
 
     if (SRC == kSrcQuant && quant_warp) {
         // ---- 2. quantise the groups of this CTA's K-block slots -------------------
@@ -552,6 +574,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
 #pragma unroll
                 for (int k = 0; k < kQuantDepth; ++k) raw[k] = nxt[k];
                 if (pass == 1 && t0 == 0 && tid == 64) FP8BS_STAMP_CLK(trec, kTpQuantFirst);
+                if (pass == 1 && warp == 0) {
+                    if (lane == 0)
+                        while (refilled < cnt &&
+                               ptx::mbar_test(&empty[refilled % S], static_cast<uint32_t>((refilled / S - 1) & 1)))
+                            refill(refilled++);
+                    __syncwarp();
+                }
             }
             asm volatile("" ::"r"(sink));
         }
@@ -615,111 +644,121 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
     if (warp == 0) {
         // ---- 1. weight ring refills ------------------------------------------------
         if (lane == 0) {
-            const uint64_t pol = ptx::policy_evict_first();
 #pragma unroll 1
-            for (int i = S; i < cnt; ++i) {
-                const int s = i % S;
-                if (!wait_bar(&empty[s], static_cast<uint32_t>((i / S - 1) & 1), p, misc)) break;
-                ptx::mbar_arrive_expect_tx(&full[s], kTileBytes);
-                ptx::bulk_g2s(sRing + s * kTileBytes, p.tiles + static_cast<size_t>(u0 + i) * kTileBytes, kTileBytes,
-                              &full[s], pol);
-                misc[kMiscIssued] = static_cast<uint32_t>(i + 1);
-                if (i - S < 8) FP8BS_STAMP_CLK(trec, kTpRefill + i - S);
+            for (int i = refilled; i < cnt; ++i) {
+                if (!wait_bar(&empty[i % S], static_cast<uint32_t>((i / S - 1) & 1), p, misc)) break;
+                refill(i);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---- 3. MMA issue ----------------------------------------------------------
-        // An mbarrier probe takes ~180 cycles to answer, about half a unit of
-        // MMA time, so the issuer probes in batches: the ring's first tiles
-        // (requested long before) once at the start, and the K-block operands
-        // four at a time; it waits on one barrier only when a batch says not
-        // yet.  The accumulator stages outnumber the units of most CTAs, so
-        // waits for the epilogue are rare.
-        if (lane == 0) {
-            bool ok = !kBlockScaled || wait_bar(sf_bar, 0, p, misc);
-            uint32_t known = 0;  // bit s: ring slot s holds its first tile; bit 16 + j: slot j's operand is ready
+        // The whole warp runs this loop, with warp-uniform values (lane 0 polls,
+        // a shuffle hands the answer to the warp), and one elected lane issues
+        // each MMA and commit: measured to issue units about twice as fast as
+        // the same loop run by lane 0 alone.  An mbarrier probe takes ~180
+        // cycles to answer, so the issuer probes in batches: the ring's first
+        // tiles (requested long before) once at the start, and the K-block
+        // operands four at a time; it waits on one barrier only when a batch
+        // says not yet.  The accumulator stages outnumber the units of most
+        // CTAs, so waits for the epilogue are rare.
+        bool ok = !kBlockScaled || warp_wait_bar(sf_bar, 0, p, misc, lane);
+        uint32_t known = 0;  // bit s: ring slot s holds its first tile; bit 16 + j: slot j's operand is ready
+        if (lane == 0)
             for (int s0 = 0; s0 < S && s0 < cnt; s0 += 4)
                 known |= ptx::mbar_test4(&full[s0], 0, &full[(s0 + 1) % S], 0, &full[(s0 + 2) % S], 0,
                                          &full[(s0 + 3) % S], 0) << s0;
-            uint32_t seg = 0, kb = kb0;  // tile segment of unit i and its K block
-            // nothing is stored to shared memory inside this loop: a generic
-            // store queued behind the MMAs' operand reads was measured to hold
-            // the thread; the count of committed units is stored once, after it
-            int committed = 0;
+        known = __shfl_sync(0xFFFFFFFFu, known, 0);
+        uint32_t seg = 0, kb = kb0;  // tile segment of unit i and its K block
+        // nothing is stored to shared memory inside this loop: a generic
+        // store queued behind the MMAs' operand reads was measured to hold
+        // the thread; the count of committed units is stored once, after it
+        int committed = 0;
 #ifdef FP8BS_TRACE
-            long long t_issue[10];
+        long long cyc[5] = {0, 0, 0, 0, 0}, t_prev = clock64();
+#define FP8BS_ISS_LAP(j)                 \
+    do {                                 \
+        const long long t_ = clock64();  \
+        cyc[j] += t_ - t_prev;           \
+        t_prev = t_;                     \
+    } while (0)
+#else
+#define FP8BS_ISS_LAP(j) ((void)0)
 #endif
 #pragma unroll 1
-            for (int i = 0; i < cnt && ok; ++i) {
-                const int s = i % S;
-                const int slot = i % p.KB;
-                const bool seg_start = i == 0 || kb == 0;
-                const int a = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) % NA);
-                const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
-                if (!kBlockScaled && !((known >> (16 + slot)) & 1u)) {
-                    const int j = slot;  // probe this slot and the next three
-                    known |= ptx::mbar_test4(&bready[j], 0, &bready[j + 1 < nslots ? j + 1 : j], 0,
-                                             &bready[j + 2 < nslots ? j + 2 : j], 0, &bready[j + 3 < nslots ? j + 3 : j], 0)
-                             << (16 + j);
-                    if (!((known >> (16 + slot)) & 1u)) {
-                        if (!wait_bar(&bready[slot], 0, p, misc)) break;
-                        known |= 1u << (16 + slot);
-                    }
+        for (int i = 0; i < cnt && ok; ++i) {
+            FP8BS_ISS_LAP(4);
+            const int s = i % S;
+            const int slot = i % p.KB;
+            const bool seg_start = i == 0 || kb == 0;
+            const int a = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) % NA);
+            const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
+            if (!kBlockScaled && !((known >> (16 + slot)) & 1u)) {
+                const int j = slot;  // probe this slot and the next three
+                uint32_t got = 0;
+                if (lane == 0)
+                    got = ptx::mbar_test4(&bready[j], 0, &bready[j + 1 < nslots ? j + 1 : j], 0,
+                                          &bready[j + 2 < nslots ? j + 2 : j], 0, &bready[j + 3 < nslots ? j + 3 : j], 0);
+                known |= __shfl_sync(0xFFFFFFFFu, got, 0) << (16 + j);
+                if (!((known >> (16 + slot)) & 1u)) {
+                    if (!warp_wait_bar(&bready[slot], 0, p, misc, lane)) break;
+                    known |= 1u << (16 + slot);
                 }
-                if (!(i < S && ((known >> i) & 1u)) && !wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc))
-                    break;
-                if ((seg_start || !kBlockScaled) && use > 0 &&
-                    !wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc))
-                    break;
+            }
+            FP8BS_ISS_LAP(0);
+            if (!(i < S && ((known >> i) & 1u)) &&
+                !warp_wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc, lane))
+                break;
+            FP8BS_ISS_LAP(1);
+            if ((seg_start || !kBlockScaled) && use > 0 &&
+                !warp_wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc, lane))
+                break;
+            FP8BS_ISS_LAP(2);
 
-                ptx::tc_fence_after();
-#ifdef FP8BS_TRACE
-                if (i < 10) t_issue[i] = clock64();
-#endif
-                const uint32_t wa = ptx::smem_addr(sRing + s * kTileBytes);
-                const uint32_t xb = ptx::smem_addr(sB + slot * C::kBBytes);
-                const uint32_t d = tmem + static_cast<uint32_t>(a * MPAD);
-                if constexpr (kBlockScaled) {
-                    const uint32_t sfa = tmem + C::kSfaCol + 4 * i;
-                    const uint32_t sfb = tmem + C::kSfbCol + 4 * slot;
+            ptx::tc_fence_after();
+            const uint32_t wa = ptx::smem_addr(sRing + s * kTileBytes);
+            const uint32_t xb = ptx::smem_addr(sB + slot * C::kBBytes);
+            const uint32_t d = tmem + static_cast<uint32_t>(a * MPAD);
+            if constexpr (kBlockScaled) {
+                const uint32_t sfa = tmem + C::kSfaCol + 4 * i;
+                const uint32_t sfb = tmem + C::kSfbCol + 4 * slot;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ptx::mma_mxf8f6f4_bs(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k),
-                                             ptx::idesc_mxf8f6f4_e4m3_e8m0(128, MPAD, k, k), sfa, sfb,
-                                             (k > 0 || !seg_start) ? 1u : 0u);
-                } else {
-                    const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
+                for (int k = 0; k < 4; ++k)
+                    ptx::mma_mxf8f6f4_bs_warp(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k),
+                                              ptx::idesc_mxf8f6f4_e4m3_e8m0(128, MPAD, k, k), sfa, sfb,
+                                              (k > 0 || !seg_start) ? 1u : 0u);
+            } else {
+                const uint32_t idesc = ptx::idesc_f8f6f4_e4m3(128, MPAD);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        ptx::mma_f8f6f4(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k), idesc,
-                                        k > 0 ? 1u : 0u);
-                }
-                ptx::mma_commit(&empty[s]);  // frees the ring slot
-                committed = i + 1;
-                const bool seg_end = ++kb == KB || i == cnt - 1;
-                // the stage's sum is complete: per unit (fp32), per segment (ue8m0).
-                // Its own barrier, not the ring's: that one can run a phase ahead
-                // before the epilogue looks; this one waits for the epilogue
-                if (!kBlockScaled || seg_end) ptx::mma_commit(&accfull[a]);
-                if (seg_end) {
-                    kb = 0;
-                    ++seg;
-                }
+                for (int k = 0; k < 4; ++k)
+                    ptx::mma_f8f6f4_warp(d, ptx::smem_desc_sw128(wa + 32 * k), ptx::smem_desc_sw128(xb + 32 * k), idesc,
+                                         k > 0 ? 1u : 0u);
             }
-            misc[kMiscCommitted] = static_cast<uint32_t>(committed);
-#ifdef FP8BS_TRACE
-            FP8BS_STAMP_CLK(trec, kTpMmaLast);
-            for (int i = 0; i < 10 && i < committed; ++i) {
-                trec[2 * (kTpMmaUnit + i)] = 1;
-                trec[2 * (kTpMmaUnit + i) + 1] = static_cast<unsigned long long>(t_issue[i]);
+            ptx::mma_commit_warp(&empty[s]);  // frees the ring slot
+            committed = i + 1;
+            const bool seg_end = ++kb == KB || i == cnt - 1;
+            // the stage's sum is complete: per unit (fp32), per segment (ue8m0).
+            // Its own barrier, not the ring's: that one can run a phase ahead
+            // before the epilogue looks; this one waits for the epilogue
+            if (!kBlockScaled || seg_end) ptx::mma_commit_warp(&accfull[a]);
+            FP8BS_ISS_LAP(3);
+            if (seg_end) {
+                kb = 0;
+                ++seg;
             }
-            if (committed > 0) {
-                trec[2 * kTpMmaFirst] = 1;
-                trec[2 * kTpMmaFirst + 1] = static_cast<unsigned long long>(t_issue[0]);
-            }
-#endif
         }
+        __syncwarp();
+        if (lane == 0) misc[kMiscCommitted] = static_cast<uint32_t>(committed);
+#ifdef FP8BS_TRACE
+        if (lane == 0) {
+            FP8BS_STAMP_CLK(trec, kTpMmaLast);
+            for (int j = 0; j < 5; ++j) {
+                trec[2 * (kTpIssCycles + j)] = 1;
+                trec[2 * (kTpIssCycles + j) + 1] = static_cast<unsigned long long>(cyc[j]);
+            }
+
+        }
+#endif
         __syncwarp();
     }
 
@@ -776,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                         }
                     }
                     ptx::tc_fence_after();
+                    if (i < 8 && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiSeen + i);
                     const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
                     const float sw = sWs[i];
                     const uint32_t* xs = sXs + (i % p.KB) * MPAD;

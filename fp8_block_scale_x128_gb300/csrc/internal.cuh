@@ -47,7 +47,7 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
 //                             first and one for the last n-tile of its range,
 //                             each [64 columns][128 rows] of tagged words
 //   then 64 x K + 64 x K/128 x 4  codes and scales of the routed two-launch
-//                             path (33 to 64 tokens) when the caller does not
+//                             path (21 to 64 tokens) when the caller does not
 //                             ask for them
 constexpr size_t kWsErrorBytes = 256;
 constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
@@ -68,7 +68,7 @@ __host__ __device__ constexpr size_t ws_total_bytes(int sm_count, int64_t K) {
 
 // Largest token count the fused kernel quantises itself; fp8bs_gemm_fused
 // runs larger calls as the quant, then the GEMM on its codes.
-constexpr int kFusedMaxM = 32;
+constexpr int kFusedMaxM = 20;
 
 // Units of work (128x128 weight tiles) one CTA of the fused kernel owns at most.
 constexpr int kMaxUnitsM16 = 12;
@@ -239,8 +239,10 @@ __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __res
 // ---------------------------------------------------------------------------
 
 cudaError_t launch_encode_e4m3(const float* v, int64_t n, uint8_t* codes, cudaStream_t stream);
+// pdl: launched with programmatic dependent launch (the kernel lets its
+// dependent start at once and waits for its predecessor before reading x).
 cudaError_t launch_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int kind,
-                         uint8_t* xq, void* xs, cudaStream_t stream);
+                         uint8_t* xq, void* xs, cudaStream_t stream, bool pdl = false);
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int kind,
                                 uint8_t* wq, void* ws, cudaStream_t stream);
 cudaError_t launch_prepack(const uint8_t* wq, int64_t ldw, const void* ws, int64_t N, int64_t K,

@@ -12,6 +12,7 @@
 // power-of-two scales per "[Perf] [AMD] dsv4: optional e8m0 mxscale GEMM for
 // dense 128x128 fp8 linears (6/8)", "Motivation").
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace fp8bs {
 namespace {
@@ -23,9 +24,16 @@ constexpr int kQuantWarps = 8;
 template <int KIND>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_1x128_kernel(const uint16_t* __restrict__ x, int M, int K, int64_t ldx,
-                       uint8_t* __restrict__ xq, void* __restrict__ xs) {
+                       uint8_t* __restrict__ xq, void* __restrict__ xs, int pdl) {
     __shared__ float2 tab[kScaleTab];
     fill_scale_table(tab, threadIdx.x, kQuantWarps * 32);
+    // programmatic dependent launch: let the next kernel (the GEMM on these
+    // codes) start its prologue now; wait for the kernel before (the producer
+    // of x) before the first read of x
+    if (pdl) {
+        ptx::griddep_launch_dependents();
+        ptx::griddep_wait();
+    }
     __syncthreads();
     const int l16 = threadIdx.x & 15;
     const int KB = K / kTile;
@@ -136,18 +144,26 @@ cudaError_t launch_encode_e4m3(const float* v, int64_t n, uint8_t* codes, cudaSt
 }
 
 cudaError_t launch_quant(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int kind,
-                         uint8_t* xq, void* xs, cudaStream_t stream) {
+                         uint8_t* xq, void* xs, cudaStream_t stream, bool pdl) {
     const int64_t groups = M * (K / kTile);
     int64_t blocks = (groups + 2 * kQuantWarps - 1) / (2 * kQuantWarps);
     if (blocks > 65535) blocks = 65535;
     if (blocks < 1) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kQuantWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int pdl_flag = pdl ? 1 : 0;
     if (kind == FP8BS_SCALE_UE8M0)
-        quant_1x128_kernel<FP8BS_SCALE_UE8M0><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(
-            x, static_cast<int>(M), static_cast<int>(K), ldx, xq, xs);
-    else
-        quant_1x128_kernel<FP8BS_SCALE_F32><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(
-            x, static_cast<int>(M), static_cast<int>(K), ldx, xq, xs);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<FP8BS_SCALE_UE8M0>, x, static_cast<int>(M),
+                                  static_cast<int>(K), ldx, xq, xs, pdl_flag);
+    return cudaLaunchKernelEx(&cfg, quant_1x128_kernel<FP8BS_SCALE_F32>, x, static_cast<int>(M), static_cast<int>(K),
+                              ldx, xq, xs, pdl_flag);
 }
 
 cudaError_t launch_quant_weight(const float* w, int64_t N, int64_t K, int64_t ldw, int kind,

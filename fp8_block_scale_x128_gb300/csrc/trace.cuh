@@ -19,7 +19,7 @@ namespace fp8bs {
 
 constexpr int kTraceCalls = 256;
 constexpr int kTraceCtas = 160;
-constexpr int kTracePoints = 48;
+constexpr int kTracePoints = 64;
 
 enum TracePoint : int {
     kTpEntry = 0,       // thread 0, first instruction
@@ -42,7 +42,13 @@ enum TracePoint : int {
     kTpEpiUnit = 26,    // + i (i < 10): epilogue warp 0, unit i accumulated
     kTpRefill = 36,     // + j (j < 8): the ring thread, the refill of unit S + j issued
     kTpMmaIssued = 44,  // + i (i < 4): the MMA issuer, unit i's commits issued
-    kTpCount = 48,
+    kTpEpiSeen = 48,    // + i (i < 8): epilogue warp 0, unit i's sum known complete (fp32 scales)
+    kTpIssCycles = 56,  // + j (j < 5): the MMA issuer's cycles summed over its loop, in the clock field:
+                        // waiting for operands, for ring tiles, for accumulator stages, issuing, the rest
+    kTpGatherLoaded = 61,  // epilogue warp 0, an owner's first round of partials all tagged
+    kTpGatherPolls = 62,   // epilogue warp 0, an owner's re-polls summed over its rounds (count, clock field)
+    kTpGatherSummed = 63,  // epilogue warp 0, an owner's sums done (before the y stores)
+    kTpCount = 64,
 };
 
 #ifdef FP8BS_TRACE

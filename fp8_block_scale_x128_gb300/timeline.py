@@ -33,11 +33,19 @@ import sys
 POINTS = (["entry", "setup", "wait", "quant_first", "quant_done", "xchg_done", "mma_first",
            "mma_last", "epi_last", "publish", "reduce_end", "teardown", "exit", "xload", "epoch",
            "gather"] + [f"mma_unit{i}" for i in range(10)] + [f"epi_unit{i}" for i in range(10)]
-          + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)])
+          + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)]
+          + [f"epi_seen{i}" for i in range(8)]
+          + ["iss_operand", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
+          + ["gather_loaded", "gather_polls", "gather_summed"])
+# points that hold a count, not a time
+COUNTS = ["gather_polls"]
+# points that hold a cycle count (a duration), not a time
+DURATIONS = ["iss_operand", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
 PHASES = (["xload", "epoch", "quant_first", "quant_done", "xchg_done", "mma_first", "mma_last",
-           "epi_last", "publish", "gather", "reduce_end", "teardown", "exit"]
+           "epi_last", "publish", "gather", "gather_loaded", "gather_summed", "reduce_end", "teardown", "exit"]
           + [f"mma_unit{i}" for i in range(10)] + [f"epi_unit{i}" for i in range(10)]
-          + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)])
+          + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)]
+          + [f"epi_seen{i}" for i in range(8)])
 
 
 def _med(v):
@@ -64,19 +72,25 @@ def analyse(tr, epochs, grid):
         span_ns = np.maximum(gt[:, E] - gt[:, N0], 1)
         ghz = (ck[:, E] - ck[:, N0]) / span_ns
         phases = {}
-        for name in PHASES:
+        for name in PHASES + DURATIONS + COUNTS:
             j = POINTS.index(name)
             have = gt[:, j] > 0
             if not have.any():
                 continue
-            dt_us = (ck[have, j] - ck[have, W]) / ghz[have] / 1e3
+            if name in COUNTS:
+                dt_us = ck[have, j].astype(np.float64)
+            elif name in DURATIONS:
+                dt_us = ck[have, j] / ghz[have] / 1e3
+            else:
+                dt_us = (ck[have, j] - ck[have, W]) / ghz[have] / 1e3
             phases[name] = (float(np.median(dt_us)), float(dt_us.max()), int(have.sum()))
         last = int(np.argmax(gt[:, E]))
         last_row = {}
-        for name in PHASES:
+        for name in PHASES + DURATIONS + COUNTS:
             j = POINTS.index(name)
-            if gt[last, j] > 0:
-                last_row[name] = float((ck[last, j] - ck[last, W]) / ghz[last] / 1e3)
+            if gt[last, j] > 0 and name not in COUNTS:
+                base = 0 if name in DURATIONS else ck[last, W]
+                last_row[name] = float((ck[last, j] - base) / ghz[last] / 1e3)
         calls.append({"entry_min": int(gt[:, N0].min()), "wait": gt[:, W], "entry": gt[:, N0],
                       "exit_max": int(gt[:, E].max()), "phases": phases, "last": last_row,
                       "ghz": float(np.median(ghz))})
@@ -100,7 +114,11 @@ def report(M, N, K, grid, calls) -> str:
     span = [(calls[i]["exit_max"] - int(calls[i]["wait"].max())) / 1e3 for i in range(1, len(calls))]
     out.append(f"  last exit after the last release   {_med(span):7.2f} us")
     out.append("  after each CTA's own release (us)   median   max    CTAs   last CTA")
-    for name in PHASES:
+    for name in PHASES + DURATIONS + COUNTS:
+        if name == COUNTS[0]:
+            out.append("  counts                               median   max    CTAs")
+        if name == DURATIONS[0]:
+            out.append("  the MMA issuer's loop, summed (us)   median   max    CTAs   last CTA")
         rows = [c["phases"][name] for c in calls[1:] if name in c["phases"]]
         if not rows:
             continue

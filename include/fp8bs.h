@@ -229,11 +229,13 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *   flags    : 0 or FP8BS_FLAG_PDL.
  * The result is deterministic: the split-K partials are summed in a fixed
  * order, so repeated calls and graph replays give identical bits.
- * Up to 39 tokens the call is one launch.  From 40 tokens on it is two: the
+ * Up to 20 tokens the call is one launch.  From 21 tokens on it is two: the
  * 1x128 quant (into xq_out / xs_out when given, else into the workspace),
  * then the GEMM on those codes, the same kernels as fp8bs_quant followed by
- * fp8bs_gemm_prequant and bit-identical to them; that pair was measured
- * faster there than the 64-token single launch.
+ * fp8bs_gemm_prequant and bit-identical to them (with FP8BS_FLAG_PDL both
+ * launch with programmatic dependent launch); the single launch quantises
+ * every K block its CTAs use in every CTA, which grows with the tokens, and
+ * the pair was measured faster from about 21 tokens on.
  * The CTAs of one launch exchange data, so a call assumes the whole device:
  * one CTA per multiprocessor, all resident together.  (Under a partition of
  * the GPU with fewer multiprocessors the bounded waits expire and the call
@@ -365,7 +367,7 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
 
 #define FP8BS_TRACE_CALLS 256  /* calls kept, by workspace epoch modulo 256  */
 #define FP8BS_TRACE_CTAS 160   /* CTAs kept per call                         */
-#define FP8BS_TRACE_POINTS 48  /* phase stamps per CTA                       */
+#define FP8BS_TRACE_POINTS 64  /* phase stamps per CTA                       */
 
 /* Copy the per-phase timeline of the fused GEMM's most recent calls to host
  * memory.  Only a library built with tracing records one (native_build's
