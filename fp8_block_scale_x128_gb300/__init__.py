@@ -32,7 +32,7 @@ FP8BS_STATIC_MAX_SMS = 160
 STATUS = {
     0: "FP8BS_OK", -1: "FP8BS_ERR_ARG", -2: "FP8BS_ERR_SHAPE", -3: "FP8BS_ERR_ALIGN",
     -4: "FP8BS_ERR_SCALE_KIND", -5: "FP8BS_ERR_WORKSPACE", -6: "FP8BS_ERR_CUDA",
-    -7: "FP8BS_ERR_TIMEOUT", -8: "FP8BS_ERR_DEVICE",
+    -7: "FP8BS_ERR_TIMEOUT", -8: "FP8BS_ERR_DEVICE", -9: "FP8BS_ERR_RESIDENCY",
 }
 globals().update({name: code for code, name in STATUS.items()})
 
@@ -111,6 +111,7 @@ def lib() -> ctypes.CDLL:
             "fp8bs_gemm_fused_static": ([vp, i64, i64, vp, sz, i64, i64, ci, vp, i64, vp, vp, vp,
                                          c.c_uint, vp], ci),
             "fp8bs_trace_read": ([vp, sz], ci),
+            "fp8bs_debug_config": ([ctypes.c_longlong, ci], ci),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -402,6 +403,13 @@ def fp8bs_trace_read():
     rc = lib().fp8bs_trace_read(ctypes.c_void_p(buf.ctypes.data), buf.nbytes)
     _check(rc, "fp8bs_trace_read")
     return buf
+
+
+def fp8bs_debug_config(timeout_cycles: int = 0, sm_count_override: int = 0) -> None:
+    """Diagnostic overrides of the fused GEMM's launches (tests only): the
+    bounded waits' limit in SM cycles and the multiprocessor count grids and
+    workspaces are sized for; 0 restores each default."""
+    _check(lib().fp8bs_debug_config(int(timeout_cycles), int(sm_count_override)), "fp8bs_debug_config")
 
 
 def fp8bs_check_error(workspace: torch.Tensor, stream=None) -> int:

@@ -35,13 +35,31 @@ bool nk_ok(int64_t N, int64_t K) {
     return N >= kTile && K >= kTile && N % kTile == 0 && K % kTile == 0 && N <= kMaxDim && K <= kMaxDim;
 }
 
-int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+int status_of(cudaError_t e) {
+    if (e == cudaSuccess) return FP8BS_OK;
+    // the launchers' refusal of a grid that cannot be resident at once
+    return e == cudaErrorCooperativeLaunchTooLarge ? FP8BS_ERR_RESIDENCY : FP8BS_ERR_CUDA;
+}
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Diagnostic overrides (fp8bs_debug_config); 0: the defaults.
+std::atomic<long long> g_timeout_override{0};
+std::atomic<int> g_sm_override{0};
+
+long long timeout_cycles() {
+    const long long t = g_timeout_override.load(std::memory_order_relaxed);
+    return t > 0 ? t : kDefaultTimeoutCycles;
+}
 
 // Multiprocessor count of the current device, cached per device (relaxed
 // atomics: concurrent first calls from several host threads may both query).
 int current_sm_count(int* out) {
+    const int forced = g_sm_override.load(std::memory_order_relaxed);
+    if (forced > 0) {
+        *out = forced;
+        return FP8BS_OK;
+    }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BS_ERR_CUDA;
     static std::atomic<int> cache[64];
@@ -139,6 +157,7 @@ const char* fp8bs_status_string(int status) {
         case FP8BS_ERR_CUDA: return "CUDA runtime error";
         case FP8BS_ERR_TIMEOUT: return "device wait timed out";
         case FP8BS_ERR_DEVICE: return "device-side check failed";
+        case FP8BS_ERR_RESIDENCY: return "the launch's CTAs cannot all be resident at once";
         default: return "unknown status";
     }
 }
@@ -295,7 +314,7 @@ int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* pack
     a.xq_out = xq_out;
     a.xs_out = xs_out;
     a.sm_count = sm;
-    a.timeout_cycles = kDefaultTimeoutCycles;
+    a.timeout_cycles = timeout_cycles();
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     return status_of(launch_fused_routed(a, as_stream(stream)));
 }
@@ -331,7 +350,7 @@ int fp8bs_gemm_prequant(const uint8_t* xq, int64_t M, int64_t ldxq, const void* 
     a.xq_out = nullptr;
     a.xs_out = nullptr;
     a.sm_count = sm;
-    a.timeout_cycles = kDefaultTimeoutCycles;
+    a.timeout_cycles = timeout_cycles();
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     a.xq_in = xq;
     a.ldxq = ldxq;
@@ -377,7 +396,7 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
     a.xq_out = xq_out;
     a.xs_out = xs_out;
     a.sm_count = sm;
-    a.timeout_cycles = kDefaultTimeoutCycles;
+    a.timeout_cycles = timeout_cycles();
     a.pdl = (flags & FP8BS_FLAG_PDL) ? 1 : 0;
     rc = status_of(launch_fused_routed(a, as_stream(stream)));
     if (rc != FP8BS_OK || !status_out) return rc;
@@ -387,6 +406,12 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
         cudaSuccess)
         return FP8BS_ERR_CUDA;
     return status_of(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), as_stream(stream)));
+}
+
+int fp8bs_debug_config(long long timeout_cycles, int sm_count_override) {
+    g_timeout_override.store(timeout_cycles > 0 ? timeout_cycles : 0, std::memory_order_relaxed);
+    g_sm_override.store(sm_count_override > 0 ? sm_count_override : 0, std::memory_order_relaxed);
+    return FP8BS_OK;
 }
 
 int fp8bs_trace_read(void* host_dst, size_t bytes) {

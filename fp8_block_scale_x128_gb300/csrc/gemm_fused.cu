@@ -890,15 +890,27 @@ cudaError_t launch_impl(const Params& p, int grid, cudaStream_t stream) {
     auto kern = fused_quant_gemm_kernel<MPAD, KIND, SRC>;
     // Opt in to the dynamic shared memory once per device (not a stream
     // operation, so it is harmless during graph capture too).
-    static std::atomic<int> configured[64];
+    // The CTAs of a launch wait for one another: refuse a grid that the
+    // device cannot hold at once (occupancy at this kernel's shared memory
+    // and threads, times the device's multiprocessors), before launching.
+    // Cached per device: resident CTAs per SM times SMs, once configured.
+    static std::atomic<int> capacity[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_relaxed)) {
+    int cap = dev >= 0 && dev < 64 ? capacity[dev].load(std::memory_order_relaxed) : 0;
+    if (cap <= 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev].store(1, std::memory_order_relaxed);
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, C::kSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cap = per_sm * sms;
+        if (dev >= 0 && dev < 64) capacity[dev].store(cap, std::memory_order_relaxed);
     }
+    if (grid > cap) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);

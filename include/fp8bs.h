@@ -68,6 +68,7 @@ typedef enum {
     FP8BS_ERR_CUDA = -6,       /* a CUDA runtime call failed (launch, copy, attribute) */
     FP8BS_ERR_TIMEOUT = -7,    /* device: a bounded wait expired; outputs are invalid */
     FP8BS_ERR_DEVICE = -8,     /* device: another device-side check failed */
+    FP8BS_ERR_RESIDENCY = -9,  /* the launch's CTAs cannot all be resident at once; nothing launched */
 } fp8bs_status;
 
 /* Largest token count of the fused GEMM.  [P1] "Motivation" fuses up to 32
@@ -195,18 +196,25 @@ enum {
 
 /* Workspace bytes the fused GEMM needs for an N x K weight on a device with
  * sm_count multiprocessors (sm_count <= 0: the current device, which needs a
- * CUDA device): a 256-byte error word, 4 KB of epoch words, 16 KB of
- * split-K flags, one 32 KB split-K slot per multiprocessor and 16.5 KB per
- * 128 columns of K for the quantised activations the CTAs exchange.  The size
- * depends on K and sm_count only and every region sits at a place that
- * depends on sm_count only, so a workspace sized for the largest K serves
- * every weight of that K or less.  Returns 0 for an
- * unsupported shape (K/128 must not exceed 10 * sm_count). */
+ * CUDA device): a 256-byte error word, 4 KB of epoch words, two 64 KB split-K
+ * partial slots per multiprocessor, and 64 x K + 64 x K/128 x 4 bytes for the
+ * codes and scales of the two-launch route when the caller does not ask for
+ * them.  The size depends on K and sm_count only and every region sits at a
+ * place that depends on sm_count only, so a workspace sized for the largest K
+ * serves every weight of that K or less.  Returns 0 for an unsupported shape
+ * (K/128 must not exceed 10 * sm_count). */
 size_t fp8bs_workspace_bytes(int64_t N, int64_t K, int sm_count);
 
 /* Zero a workspace before its first use.  The fused GEMM tags every word it
  * exchanges through the workspace with a per-call epoch kept in the workspace
- * itself, so later calls and graph replays need no re-init. */
+ * itself, so later calls and graph replays need no re-init.  The epoch is a
+ * 32-bit counter that skips 0 (the tag of a word never written since the
+ * init) when it wraps, so its period is 2^32 - 1 calls.  A stale word is
+ * taken for current only if it was last written a whole number of periods
+ * before and not since: calls of one shape rewrite every word they read, so
+ * that needs a word left idle (a larger M or another split of the same
+ * workspace) for exactly that many calls; a re-init before reusing a
+ * workspace across such spans rules it out. */
 int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Y = bf16(x W^T) with the 1x128 activation quant fused in.
@@ -237,11 +245,16 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  * every K block its CTAs use in every CTA, which grows with the tokens, and
  * the pair was measured faster from about 21 tokens on.
  * The CTAs of one launch exchange data, so a call assumes the whole device:
- * one CTA per multiprocessor, all resident together.  (Under a partition of
- * the GPU with fewer multiprocessors the bounded waits expire and the call
- * reports FP8BS_ERR_TIMEOUT.)
- * Errors (host): ARG, SHAPE, ALIGN, WORKSPACE, CUDA.  Errors (device, via
- * fp8bs_check_error): SCALE_KIND (header mismatch; y not written), TIMEOUT. */
+ * one CTA per multiprocessor, all resident together.  Before each launch the
+ * library checks that the kernel's occupancy (CTAs per multiprocessor at its
+ * shared memory and thread count) times the device's multiprocessors covers
+ * the grid, and returns FP8BS_ERR_RESIDENCY without launching if not.  It
+ * cannot see kernels of other streams or processes that hold
+ * multiprocessors: there the bounded waits expire and the call reports
+ * FP8BS_ERR_TIMEOUT.
+ * Errors (host): ARG, SHAPE, ALIGN, WORKSPACE, CUDA, RESIDENCY.  Errors
+ * (device, via fp8bs_check_error): SCALE_KIND (header mismatch; y not
+ * written), TIMEOUT. */
 int fp8bs_gemm_fused(const uint16_t* x, int64_t M, int64_t ldx, const void* packed,
                      size_t packed_bytes, int64_t N, int64_t K, int scale_kind, uint16_t* y,
                      int64_t ldy, void* workspace, size_t workspace_bytes, uint8_t* xq_out,
@@ -382,6 +395,28 @@ int fp8bs_gemm_fused_static(const uint16_t* x, int64_t M, int64_t ldx, const voi
  * Synchronises with the device (a blocking copy).  Errors: FP8BS_ERR_ARG (no
  * tracing in this build, or a null buffer), FP8BS_ERR_CUDA. */
 int fp8bs_trace_read(void* host_dst, size_t bytes);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostic settings (for the library's own tests; no counterpart on the  */
+/* pages)                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Override, for the calls that follow in this process, two settings of the
+ * fused GEMM's launches:
+ *   timeout_cycles   : the limit of every bounded wait inside the kernel, in
+ *                      SM clock cycles; <= 0 restores the default (2e9,
+ *                      about 1 s), which is set far above any legitimate wait.
+ *                      A short limit (1e5 .. 1e6) makes a wait that cannot
+ *                      complete expire quickly, so a test can drive the
+ *                      expiry path (FP8BS_ERR_TIMEOUT, drain, return).
+ *   sm_count_override: the multiprocessor count the library sizes grids and
+ *                      workspaces for; <= 0 restores the device's own.  The
+ *                      residency check still uses the device's real count, so
+ *                      a large override makes a call return
+ *                      FP8BS_ERR_RESIDENCY without launching.
+ * Process-wide, not synchronised with calls in flight on other host threads.
+ * Returns FP8BS_OK. */
+int fp8bs_debug_config(long long timeout_cycles, int sm_count_override);
 
 #ifdef __cplusplus
 }

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_function(L):
 
 def test_version_and_status_strings(L):
     assert fb.fp8bs_version() >> 16 == 1
-    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9):
         assert fb.fp8bs_status_string(s) and fb.fp8bs_status_string(s) != "unknown status"
     assert fb.fp8bs_status_string(-99) == "unknown status"
 

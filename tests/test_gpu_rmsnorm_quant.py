@@ -159,3 +159,23 @@ def test_rmsnorm_quant_full_size_sampled_rows(dev, oracle_mod):
     y = H.torch_u16_to_np(yd.index_select(0, idx))
     check_against_oracle(oracle_mod, x, g, EPS, F32, xq.index_select(0, idx).cpu().numpy(),
                          xs.index_select(0, idx).cpu().numpy(), y, "16384x7168 sampled rows")
+
+
+@pytest.mark.parametrize("kind", [F32, UE8])
+def test_rmsnorm_quant_codes_equal_the_oracle_producer(dev, oracle_mod, kind):
+    # End to end against the oracle's own producer (oracle.rmsnorm_quant, which
+    # quantises its own bf16(y64)): wherever the kernel's normalised row equals
+    # the oracle's in every element -- the premise, asserted first to hold for
+    # most rows -- its codes and scales must equal the oracle's byte for byte.
+    M, K = 96, 256
+    x = synth.x_bf16(M, K, seed=9001 + kind)
+    g = synth.gamma_bf16(K, seed=9002 + kind)
+    yd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    xq, xs, yd = fb.fp8bs_rmsnorm_quant(bf16_dev(x, dev), bf16_dev(g, dev), EPS, kind, y=yd)
+    torch.cuda.synchronize()
+    y = H.torch_u16_to_np(yd)
+    y_o, q_o, s_o = oracle_mod.rmsnorm_quant(x, g, EPS, kind)
+    rows = np.flatnonzero((y == y_o).all(axis=1))
+    assert rows.size >= 3 * M // 4, f"premise: only {rows.size} of {M} rows have y == bf16(y64)"
+    assert np.array_equal(xq.cpu().numpy()[rows], q_o[rows])
+    assert np.array_equal(xs.cpu().numpy()[rows], s_o[rows])

@@ -40,10 +40,12 @@ def quant_outs(M, K, kind, dev):
 
 
 @pytest.mark.parametrize("M,N,K,kind,pdl", [
-    (5, 5120, 4096, F32, False),      # local activation quant
-    (17, 4096, 2048, UE8, False),     # quant distributed over the CTAs
-    (32, 1536, 7168, UE8, True),      # PDL launches
-    (24, 16384, 8192, F32, False),    # several launches of 128-row slices
+    (5, 5120, 4096, F32, False),      # one launch, 16-token tile
+    (17, 4096, 2048, UE8, False),     # one launch, 32-token tile
+    (32, 1536, 7168, UE8, True),      # two launches (quant into the scratch, GEMM on it), PDL
+    (24, 16384, 8192, F32, False),    # two launches, the GEMM split over n-tile slices
+    (40, 5120, 4096, F32, False),     # two launches, 64-token tile
+    (64, 1536, 7168, UE8, True),      # two launches, 64-token tile, PDL
 ])
 def test_static_scratch_matches_workspace_call_twice(dev, M, N, K, kind, pdl):
     x = synth.x_bf16_torch(M, K, seed=77 * M + K, device=dev)
