@@ -20,9 +20,13 @@ scales; *1 for e8m0) + 2*M*K (bf16 x) + 2*M*N (bf16 y).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload msweep|smallest|shapes|ue8m0|chain4|chain16|chain32]
 
+The default run also times every other workload (key "workloads": smallest,
+shapes, ue8m0, chain4/16/32) and the M sweep per M.
+
 --impl reference times the CPU oracle (the plain restatement of the method the
-tests compare against) on this host's cores: each step computes one 128-row
-slice of the weight for every call of the step's distinct shapes.  Under
+tests compare against) on this host's cores: each step computes one whole
+call of the workload (its distinct calls in turn), so its GB/s is that of
+whole weights.  Under
 torchrun (N > 1) every rank runs its own replica on its own GPU (each rank
 stands for one tensor-parallel shard: the pages' shapes are per-rank shapes),
 the timed region is bracketed by barriers, and the slowest rank's time counts.
@@ -242,6 +246,13 @@ class OracleSample:
                     synth.w_f32(N, K, seed=N + K), kind)
             self.x[(M, K)] = synth.x_bf16(M, K, seed=M + K)
 
+    def whole_call(self, i: int) -> int:
+        """The i-th distinct call (cyclically) on its whole weight; returns bytes."""
+        M, N, K, kind = self.calls[i % len(self.calls)]
+        wq, ws = self.w[(N, K, kind)]
+        self.oracle.linear(self.x[(M, K)], wq, ws, kind, nthreads=self.cores)
+        return algorithmic_bytes(M, N, K, kind)
+
     def step(self, i: int, n_tiles: int = 1) -> int:
         """Every distinct call on n_tiles consecutive 128-row slices; returns bytes."""
         nbytes = 0
@@ -267,21 +278,28 @@ def run_reference(args):
         return 0
     desc, calls = workload_plan(args.workload)
     smp = OracleSample(calls)
+    # one step = one whole call of the workload (its distinct calls in turn),
+    # so the GB/s is that of whole weights, like the main arm's cpu_baseline
     for i in range(args.warmup):
-        smp.step(i)
+        smp.whole_call(i)
     nbytes = 0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        nbytes += smp.step(args.warmup + i)
+        nbytes += smp.whole_call(args.warmup + i)
     el = time.perf_counter() - t0
     value = nbytes / el / 1e9
+    config = bench_config(desc, calls)
+    config["calls_per_step"] = 1
+    config["reference_step"] = (f"one whole call per step: the {len(smp.calls)} distinct calls "
+                                f"{[c[:3] for c in smp.calls]} in turn, each on its whole weight")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": bench_config(desc, calls),
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": smp.cores, "kind": "oracle",
-                         "sample": smp.sample_desc(1)},
+                         "sample": config["reference_step"] + f"; oracle 1x128 quant + fp64 "
+                                   f"GEMM on {smp.cores} threads"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -328,14 +346,33 @@ class Step:
         max_n = max(c[1] for c in calls)
         max_k = max(c[2] for c in calls)
         self.workspace = fb.new_workspace(max_n, max_k, dev)
-        # one x per (M, K); with host I/O one device x per call (each call copies its own)
+        # one x per (M, K) and one y per (M, N); with host I/O every call has its
+        # own x and y, views of one device buffer each, so a step moves all of
+        # its inputs in one host->device copy and all of its outputs in one
+        # device->host copy
         self.x = {}
-        for i, (M, N, K, kind, wid) in enumerate(calls):
-            key = i if io else (M, K)
-            if key not in self.x:
-                self.x[key] = synth.x_bf16_torch(M, K, seed=31 * i + M, device=dev)
-        self.y = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-                  for (M, N, K, _k, _w) in calls}
+        self.y = {}
+        if io:
+            x_sizes = [M * K for (M, N, K, _k, _w) in calls]
+            y_sizes = [M * N for (M, N, K, _k, _w) in calls]
+            self.x_all = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
+            self.y_all = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
+            xo = yo = 0
+            for i, (M, N, K, kind, wid) in enumerate(calls):
+                self.x[i] = self.x_all[xo:xo + M * K].view(M, K)
+                self.x[i].copy_(synth.x_bf16_torch(M, K, seed=31 * i + M, device=dev))
+                self.y[i] = self.y_all[yo:yo + M * N].view(M, N)
+                xo += M * K
+                yo += M * N
+            self.x_host = torch.empty(self.x_all.numel(), dtype=torch.bfloat16).pin_memory()
+            self.x_host.copy_(self.x_all.cpu())
+            self.y_host = torch.empty(self.y_all.numel(), dtype=torch.bfloat16).pin_memory()
+        else:
+            for i, (M, N, K, kind, wid) in enumerate(calls):
+                if (M, K) not in self.x:
+                    self.x[(M, K)] = synth.x_bf16_torch(M, K, seed=31 * i + M, device=dev)
+                if (M, N) not in self.y:
+                    self.y[(M, N)] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         self.io = io
         self.pdl = pdl
         # the two-launch path: fp8bs_quant, then fp8bs_gemm_prequant on its output
@@ -346,13 +383,6 @@ class Step:
             self.xs = {(M, K, kind): torch.empty((M, K // 128), device=dev,
                                                  dtype=torch.uint8 if kind == 1 else torch.float32)
                        for (M, N, K, kind, _w) in calls}
-        if io:
-            self.x_host = [torch.empty((c[0], c[2]), dtype=torch.bfloat16).pin_memory()
-                           for c in calls]
-            for i, c in enumerate(calls):
-                self.x_host[i].copy_(self.x[i].cpu())
-            self.y_host = [torch.empty((c[0], c[1]), dtype=torch.bfloat16).pin_memory()
-                           for c in calls]
         self.stream = stream
         self.fb = fb
         # weights, x and the workspace's initial zeros were written on the current
@@ -377,21 +407,21 @@ class Step:
                 self.enqueue()
 
     def enqueue(self):
+        if self.io:
+            self.x_all.copy_(self.x_host, non_blocking=True)
         for i, (M, N, K, kind, wid) in enumerate(self.calls):
             x = self.x[i] if self.io else self.x[(M, K)]
-            y = self.y[(M, N)]
-            if self.io:
-                x.copy_(self.x_host[i], non_blocking=True)
+            y = self.y[i] if self.io else self.y[(M, N)]
             if self.two_launch:
                 xq, xs = self.xq[(M, K)], self.xs[(M, K, kind)]
                 self.fb.fp8bs_quant(x, kind, xq=xq, xs=xs, stream=self.stream)
                 self.fb.fp8bs_gemm_prequant(xq, xs, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
-                                            workspace=self.workspace, stream=self.stream)
+                                            workspace=self.workspace, pdl=self.pdl, stream=self.stream)
             else:
                 self.fb.fp8bs_gemm_fused(x, self.packs[(N, K, kind, wid)], N, K, kind, y=y,
                                          workspace=self.workspace, pdl=self.pdl, stream=self.stream)
-            if self.io:
-                self.y_host[i].copy_(y, non_blocking=True)
+        if self.io:
+            self.y_host.copy_(self.y_all, non_blocking=True)
 
 
 def time_steps(torch, step: Step, steps: int, warmup: int, world: int, dev) -> float:
@@ -413,6 +443,31 @@ def time_steps(torch, step: Step, steps: int, warmup: int, world: int, dev) -> f
 
 
 M_ABOVE_32 = [33, 48, 64]
+OTHER_WORKLOADS = ["smallest", "shapes", "ue8m0", "chain4", "chain16", "chain32"]
+
+
+def workloads_table(fb, torch, dev, stream, pdl, peak: float, target_s: float = 0.25):
+    """us/call, GB/s and fraction of the peak of every other workload of the
+    benchmark (graph replay, the same timing rules as the M sweep)."""
+    out = {}
+    for name in OTHER_WORKLOADS:
+        desc, calls = workload_plan(name)
+        step_bytes = sum(algorithmic_bytes(M, N, K, kind) for (M, N, K, kind, _) in calls)
+        progress(f"workload {name}")
+        st = Step(fb, torch, calls, dev, stream, pdl=pdl)
+        probe = time_steps(torch, st, 3, 3, 1, dev) / 3
+        reps = max(5, min(500, int(target_s * 1e3 / max(probe, 1e-3))))
+        ms = time_steps(torch, st, reps, 3, 1, dev)
+        rc = fb.fp8bs_check_error(st.workspace, stream)
+        if rc != 0:
+            raise SystemExit(f"workload {name}: device error {fb.fp8bs_status_string(rc)}")
+        gbps = step_bytes * reps / (ms / 1e3) / 1e9
+        out[name] = {"workload": desc, "calls_per_step": len(calls), "steps": reps,
+                     "us_per_call": round(ms * 1e3 / (reps * len(calls)), 3),
+                     "GBps": round(gbps, 1), "frac": round(gbps / peak, 4)}
+        del st
+        torch.cuda.empty_cache()
+    return out
 
 
 def per_m_table(fb, torch, dev, stream, pdl, two_launch=False, ms=None):
@@ -614,8 +669,9 @@ def run_gpu(args):
     del st
     torch.cuda.empty_cache()
 
-    # end to end through the public call with host buffers: every call copies
-    # its x from pinned host memory and its y back, inside the timed region
+    # end to end through the public call with host buffers: each step copies
+    # all of its calls' x from pinned host memory and all of their y back,
+    # inside the timed region
     progress("end-to-end step")
     st_io = Step(fb, torch, calls, dev, stream, io=True, pdl=pdl)
     e2e_steps = max(3, args.steps // 4)
@@ -638,6 +694,10 @@ def run_gpu(args):
                                               ms=M_ABOVE_32)}
 
     peak, peak_src = hbm_peak()
+
+    others = None
+    if args.workload == "msweep" and rank == 0 and not args.no_workloads:
+        others = workloads_table(fb, torch, dev, stream, pdl, peak)
 
     producer = None
     if rank == 0 and not args.no_producer:
@@ -666,6 +726,7 @@ def run_gpu(args):
             "per_m_us_and_GBps": per_m,
             "per_m_two_launch_us_and_GBps": per_m_two,
             "m_above_32_us_and_GBps": above_32,
+            "workloads": others,
             "producer_rmsnorm_quant": producer,
             "moe_w8a16": moe,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -675,8 +736,9 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "path": "per call: pinned host x -> device, fp8bs_gemm_fused, device y -> "
-                            "pinned host; one CUDA graph per step"},
+                    "path": "per step: one copy of every call's x from pinned host memory, the "
+                            "step's fp8bs_gemm_fused calls, one copy of every call's y to pinned "
+                            "host memory; one CUDA graph per step"},
             "gpu_launches": launches,
             "clocks": clocks,
         }
@@ -697,6 +759,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-m", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the table of the other workloads (smallest, shapes, ue8m0, chains)")
     ap.add_argument("--no-producer", action="store_true",
                     help="skip the RMSNorm + quant producer's table")
     ap.add_argument("--producer-only", action="store_true",
