@@ -439,11 +439,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                           &full[i], pol);
         }
         misc[kMiscIssued] = static_cast<uint32_t>(pre);
-        // the tiles that wait for a ring slot: start their HBM reads now, so
-        // the refills find them in L2 (they are contiguous: n-major units)
-        if (cnt > pre)
-            ptx::bulk_prefetch_l2(p.tiles + static_cast<size_t>(u0 + pre) * kTileBytes,
-                                  static_cast<uint32_t>(cnt - pre) * kTileBytes);
+        // (no L2 prefetch of the tiles beyond the ring: measured not to pay, a
+        // bulk prefetch sits in the SM's memory queue ahead of later loads)
     }
 
     if (warp == 1) {
