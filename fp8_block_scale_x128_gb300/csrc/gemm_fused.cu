@@ -149,7 +149,16 @@ struct Params {
     int pdl;
 };
 
-enum : int { kMiscTmem = 0, kMiscAbort = 1, kMiscHdrOk = 2, kMiscIssued = 3, kMiscCommitted = 4 };
+enum : int {
+    kMiscTmem = 0,
+    kMiscAbort = 1,
+    kMiscHdrOk = 2,
+    kMiscIssued = 3,
+    kMiscCommitted = 4,
+    kMiscC0 = 5,      // + segment (2): the first contributor of the segment's n-tile
+    kMiscC1 = 7,      // + segment (2): the last contributor
+    kMiscWhich0 = 9,  // + segment (2): the first contributor's partial slot for that n-tile (0 or 1)
+};
 
 __device__ __forceinline__ uint32_t unit_begin(uint32_t c, uint32_t T, uint32_t G) {
     return static_cast<uint32_t>(static_cast<uint64_t>(c) * T / G);
@@ -226,11 +235,12 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, long long
     }
 }
 
-// Word offset (from p.slots) of CTA b's partial slot for n-tile nt: slot 0
-// if nt is the tile of b's first unit, else slot 1 (its last tile).
-__device__ __forceinline__ uint32_t slot_offset(const Params& p, uint32_t b, uint32_t nt, uint32_t G) {
-    const uint32_t which = unit_begin(b, p.T, G) / static_cast<uint32_t>(p.KB) == nt ? 0u : 1u;
-    return (b * kSlotsPerCta + which) * static_cast<uint32_t>(kSlotWords);
+// Word offset (from p.slots) of CTA b's partial slot for an n-tile: slot 0
+// if the tile holds b's first unit, else slot 1 (its last tile).  Of a
+// tile's contributors c0..c1 only c0 can start before the tile, so which is
+// 0 for every b > c0 and which0 (from the set-up) for c0.
+__device__ __forceinline__ uint32_t slot_offset(uint32_t b, uint32_t c0, uint32_t which0) {
+    return (b * kSlotsPerCta + (b == c0 ? which0 : 0u)) * static_cast<uint32_t>(kSlotWords);
 }
 
 // Output of one n-tile segment by one epilogue warp: its 32 rows r = q*32 +
@@ -249,8 +259,8 @@ __device__ __forceinline__ uint32_t slot_offset(const Params& p, uint32_t b, uin
 // offsets, then its own values and the running sums of the owned columns.
 template <int MPAD>
 __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, const float (&acc)[MPAD], uint32_t c,
-                                              uint32_t c0, uint32_t c1, uint32_t G, int q, int lane, uint32_t epoch,
-                                              volatile uint32_t* misc, float* stage) {
+                                              uint32_t c0, uint32_t c1, uint32_t which0, int q, int lane,
+                                              uint32_t epoch, volatile uint32_t* misc, float* stage) {
     const int r = q * 32 + lane;
     uint16_t* yrow = p.y + static_cast<size_t>(nt) * kTile + r;
     if (c0 == c1) {
@@ -263,7 +273,7 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     const int s = static_cast<int>(c - c0);
     const int m_lo = c == c1 ? p.M : s * p.M / owners;
     const int m_hi = c == c1 ? p.M : (s + 1) * p.M / owners;
-    uint64_t* mine = p.slots + slot_offset(p, c, nt, G) + r;
+    uint64_t* mine = p.slots + slot_offset(c, c0, which0) + r;
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
         if (m < p.M && (m < m_lo || m >= m_hi)) st_word(mine + m * kTile, tag(__float_as_uint(acc[m]), epoch));
@@ -281,7 +291,7 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
 #pragma unroll 1
     for (int j = lane; j < owners; j += 32) {
         const uint32_t b = c0 + static_cast<uint32_t>(j) + (c0 + static_cast<uint32_t>(j) >= c ? 1u : 0u);
-        tab[j] = slot_offset(p, b, nt, G) + static_cast<uint32_t>(m_lo * kTile);
+        tab[j] = slot_offset(b, c0, which0) + static_cast<uint32_t>(m_lo * kTile);
     }
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
@@ -294,6 +304,12 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     const int nw = owners * width;
     constexpr int kRound = 16;
     bool ok = true;
+#ifdef FP8BS_TRACE
+    if (q == 0 && lane == 0) {
+        volatile unsigned long long* rec = reinterpret_cast<volatile unsigned long long*>(misc + 16);
+        FP8BS_STAMP_CLK(rec, kTpEpoch);  // the gather's set-up done, its loads about to go out
+    }
+#endif
 #pragma unroll 1
     for (int base = 0; base < nw && ok; base += kRound) {
         uint32_t off[kRound];
@@ -309,10 +325,24 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
             }
         }
         const long long t0 = clock64();
+#ifdef FP8BS_TRACE
+        bool first_check = true;
+#endif
         while (true) {
             bool all = true;
 #pragma unroll
             for (int k = 0; k < kRound; ++k) all = all && tagged(w[k], epoch);
+#ifdef FP8BS_TRACE
+            if (q == 0 && lane == 0) {
+                volatile unsigned long long* rec = reinterpret_cast<volatile unsigned long long*>(misc + 16);
+                if (first_check && base == 0) FP8BS_STAMP_CLK(rec, kTpGatherLoaded);  // first words back
+                if (!all) {
+                    rec[2 * kTpGatherPolls] = 1;
+                    rec[2 * kTpGatherPolls + 1] = rec[2 * kTpGatherPolls + 1] + 1;
+                }
+            }
+            first_check = false;
+#endif
             if (all) break;
             if (misc[kMiscAbort] != 0) {
                 ok = false;
@@ -345,6 +375,12 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         }
     }
     if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+#ifdef FP8BS_TRACE
+    if (q == 0 && lane == 0) {
+        volatile unsigned long long* rec = reinterpret_cast<volatile unsigned long long*>(misc + 16);
+        FP8BS_STAMP_CLK(rec, kTpGatherSummed);
+    }
+#endif
 #pragma unroll 1
     for (int col = 0; col < width; ++col) yrow[(m_lo + col) * p.ldy] = f32_to_bf16_rn(sum[col * 32 + lane]);
     return true;
@@ -463,6 +499,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         const PackedHeader* h = reinterpret_cast<const PackedHeader*>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->n == p.N && h->k == p.K &&
                         h->scale_kind == p.kind && h->tile_bytes == kTileBytes;
+        // the contributors of this CTA's (at most two) n-tiles: their 64-bit
+        // divisions here, before the wait on the previous kernel
+        for (uint32_t sg = 0; sg < 2; ++sg) {
+            const uint32_t nt = nt0 + sg;
+            const uint32_t a = cta_of(nt * KB, p.T, G);
+            misc[kMiscC0 + sg] = a;
+            misc[kMiscC1 + sg] = cta_of(nt * KB + KB - 1 < p.T ? nt * KB + KB - 1 : p.T - 1, p.T, G);
+            misc[kMiscWhich0 + sg] = unit_begin(a, p.T, G) / KB == nt ? 0u : 1u;
+        }
         misc[kMiscHdrOk] = ok ? 1u : 0u;
         ptx::mbar_arrive(hdr_bar);  // release: the epilogue reads the flag after waiting here
     }
@@ -834,10 +879,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 if (!ok) break;
             }
             if (ib == cnt && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiLast);
-            // the tile's contributors; an owner's segment is always the CTA's last
-            const uint32_t c0 = cta_of(nt * KB, p.T, G), c1 = cta_of(nt * KB + KB - 1, p.T, G);
+            // the tile's contributors (from the set-up); an owner's segment is
+            // always the CTA's last
+            const uint32_t c0 = misc[kMiscC0 + (seg & 1)], c1 = misc[kMiscC1 + (seg & 1)];
             if (hdr_ok)
-                ok = flush_segment<MPAD>(p, nt, acc, c, c0, c1, G, q, lane, epoch, misc,
+                ok = flush_segment<MPAD>(p, nt, acc, c, c0, c1, misc[kMiscWhich0 + (seg & 1)], q, lane, epoch, misc,
                                          reinterpret_cast<float*>(sRing) + q * C::kStageFloats);
             if (tid == 128) FP8BS_STAMP_CLK(trec, c == c1 && c0 != c1 ? kTpPublish : kTpReduceEnd);
             ++seg;
