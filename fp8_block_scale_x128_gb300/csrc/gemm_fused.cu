@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 raw[k] = make_uint4(0x3F8A3F81u + k, 0x3F933FA5u, 0xBF853F99u, 0x3FC13F87u);
                 if (pass == 1 && g < ng) {
                     const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
-                    const uint32_t kb = (kb0 + i) % KB;
+                    const uint32_t kb = kb0 + i < KB ? kb0 + i : kb0 + i - KB;  // i < KB, kb0 < KB
                     raw[k] = ptx::ld_global_v4(p.x + m * p.ldx + kb * kTile + l16 * 8);
                 }
             }
@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                     nxt[k] = raw[k];
                     if (pass == 1 && g2 < ng) {
                         const uint32_t i2 = div_m(static_cast<uint32_t>(g2), p.mdiv), m2 = g2 - i2 * p.M;
-                        const uint32_t kb2 = (kb0 + i2) % KB;
+                        const uint32_t kb2 = kb0 + i2 < KB ? kb0 + i2 : kb0 + i2 - KB;
                         nxt[k] = ptx::ld_global_v4(p.x + m2 * p.ldx + kb2 * kTile + l16 * 8);
                     }
                 }
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
 #pragma unroll 1
         for (int g = qt; g < ng; g += kQuantThreads) {
             const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
-            const uint32_t kb = (kb0 + i) % KB;
+            const uint32_t kb = kb0 + i < KB ? kb0 + i : kb0 + i - KB;
             const uint8_t* src = p.xq_in + m * p.ldxq + kb * kTile;
             uint8_t* row = sB + i * C::kBBytes + (m >> 3) * 1024 + (m & 7) * 128;
 #pragma unroll
@@ -712,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                                          &full[(s0 + 3) % S], 0) << s0;
         known = __shfl_sync(0xFFFFFFFFu, known, 0);
         uint32_t seg = 0, kb = kb0;  // tile segment of unit i and its K block
+        int islot = 0;               // unit i's K-block slot, i % KB
         // nothing is stored to shared memory inside this loop: a generic
         // store queued behind the MMAs' operand reads was measured to hold
         // the thread; the count of committed units is stored once, after it
@@ -731,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         for (int i = 0; i < cnt && ok; ++i) {
             FP8BS_ISS_LAP(4);
             const int s = i % S;
-            const int slot = i % p.KB;
+            const int slot = islot;  // i % KB, kept by increments (no division in this loop)
             const bool seg_start = i == 0 || kb == 0;
             const int a = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) % NA);
             const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
@@ -778,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
             }
             ptx::mma_commit_warp(&empty[s]);  // frees the ring slot
             committed = i + 1;
+            if (++islot == p.KB) islot = 0;
             const bool seg_end = ++kb == KB || i == cnt - 1;
             // the stage's sum is complete: per unit (fp32), per segment (ue8m0).
             // Its own barrier, not the ring's: that one can run a phase ahead
@@ -811,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         float acc[MPAD];
         uint32_t seg = 0;
         int i = 0, seen = 0;  // seen: units whose MMAs are known to be complete
+        int xslot = 0;        // unit i's K-block slot, i % KB (fp32 scales)
         bool ok = true;
 #pragma unroll 1
         while (i < cnt && ok) {
@@ -860,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                     if (i < 8 && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiSeen + i);
                     const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
                     const float sw = sWs[i];
-                    const uint32_t* xs = sXs + (i % p.KB) * MPAD;
+                    const uint32_t* xs = sXs + xslot * MPAD;
+                    if (++xslot == p.KB) xslot = 0;
 #pragma unroll
                     for (int h = 0; h < MPAD / 16; ++h) {
                         uint32_t rr[16];
