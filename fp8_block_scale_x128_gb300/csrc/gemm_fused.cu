@@ -158,6 +158,8 @@ enum : int {
     kMiscC0 = 5,      // + segment (2): the first contributor of the segment's n-tile
     kMiscC1 = 7,      // + segment (2): the last contributor
     kMiscWhich0 = 9,  // + segment (2): the first contributor's partial slot for that n-tile (0 or 1)
+    kMiscMlo = 11,    // + segment (2): the first column this CTA owns of that n-tile's output
+    kMiscMhi = 13,    // + segment (2): one past the last
 };
 
 __device__ __forceinline__ uint32_t unit_begin(uint32_t c, uint32_t T, uint32_t G) {
@@ -259,8 +261,8 @@ __device__ __forceinline__ uint32_t slot_offset(uint32_t b, uint32_t c0, uint32_
 // offsets, then its own values and the running sums of the owned columns.
 template <int MPAD>
 __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, const float (&acc)[MPAD], uint32_t c,
-                                              uint32_t c0, uint32_t c1, uint32_t which0, int q, int lane,
-                                              uint32_t epoch, volatile uint32_t* misc, float* stage) {
+                                              uint32_t c0, uint32_t c1, uint32_t which0, int m_lo, int m_hi, int q,
+                                              int lane, uint32_t epoch, volatile uint32_t* misc, float* stage) {
     const int r = q * 32 + lane;
     uint16_t* yrow = p.y + static_cast<size_t>(nt) * kTile + r;
     if (c0 == c1) {
@@ -271,8 +273,6 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     }
     const int owners = static_cast<int>(c1 - c0);
     const int s = static_cast<int>(c - c0);
-    const int m_lo = c == c1 ? p.M : s * p.M / owners;
-    const int m_hi = c == c1 ? p.M : (s + 1) * p.M / owners;
     uint64_t* mine = p.slots + slot_offset(c, c0, which0) + r;
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
@@ -311,10 +311,11 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     }
 #endif
 #pragma unroll 1
+    int jr = 0, colr = 0;  // word `base` = column colr of the jr-th other contributor
     for (int base = 0; base < nw && ok; base += kRound) {
         uint32_t off[kRound];
         uint64_t w[kRound];
-        int j = base / width, col = base - j * width;
+        int j = jr, col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
             off[k] = base + k < nw ? tab[j] + static_cast<uint32_t>(col * kTile + r) : 0u;
@@ -359,8 +360,8 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         }
         // running sums in CTA order: the own partial enters just before the
         // first other contributor that follows this CTA (j == s)
-        j = base / width;
-        col = base - j * width;
+        j = jr;
+        col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
             if (base + k < nw) {
@@ -373,6 +374,8 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
                 ++j;
             }
         }
+        jr = j;  // the next round starts where this one ended
+        colr = col;
     }
     if (__any_sync(0xFFFFFFFFu, !ok)) return false;
 #ifdef FP8BS_TRACE
@@ -507,6 +510,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
             misc[kMiscC0 + sg] = a;
             misc[kMiscC1 + sg] = cta_of(nt * KB + KB - 1 < p.T ? nt * KB + KB - 1 : p.T - 1, p.T, G);
             misc[kMiscWhich0 + sg] = unit_begin(a, p.T, G) / KB == nt ? 0u : 1u;
+            // owned columns: contributor s = c - c0 of the c1 - c0 owners (none for c1)
+            const uint32_t b1 = misc[kMiscC1 + sg];
+            const int owners = static_cast<int>(b1 - a), sc = static_cast<int>(c - a);
+            const bool owner = c != b1 && owners > 0;
+            misc[kMiscMlo + sg] = static_cast<uint32_t>(owner ? sc * p.M / owners : p.M);
+            misc[kMiscMhi + sg] = static_cast<uint32_t>(owner ? (sc + 1) * p.M / owners : p.M);
         }
         misc[kMiscHdrOk] = ok ? 1u : 0u;
         ptx::mbar_arrive(hdr_bar);  // release: the epilogue reads the flag after waiting here
@@ -887,7 +896,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
             // always the CTA's last
             const uint32_t c0 = misc[kMiscC0 + (seg & 1)], c1 = misc[kMiscC1 + (seg & 1)];
             if (hdr_ok)
-                ok = flush_segment<MPAD>(p, nt, acc, c, c0, c1, misc[kMiscWhich0 + (seg & 1)], q, lane, epoch, misc,
+                ok = flush_segment<MPAD>(p, nt, acc, c, c0, c1, misc[kMiscWhich0 + (seg & 1)],
+                                         static_cast<int>(misc[kMiscMlo + (seg & 1)]),
+                                         static_cast<int>(misc[kMiscMhi + (seg & 1)]), q, lane, epoch, misc,
                                          reinterpret_cast<float*>(sRing) + q * C::kStageFloats);
             if (tid == 128) FP8BS_STAMP_CLK(trec, c == c1 && c0 != c1 ? kTpPublish : kTpReduceEnd);
             ++seg;
