@@ -122,19 +122,6 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float (&v)[8]) {
 }
 
 // Codes of the IEEE quotients RN32(v / scale) for the 8 bf16 values in raw.
-// Out of line, all arguments by value: the rare path of quant_slice.
-static __device__ __noinline__ uint2 e4m3_codes8_divide(uint4 raw, float scale) {
-    float v[8];
-    unpack_bf16x8(raw, v);
-    float q[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], scale);
-    uint2 c;
-    c.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-    c.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
-    return c;
-}
-
 // Scale table.  A group maximum amax is a bf16 value m * 2^e with
 // m = 1 + i/128 (7 mantissa bits), so its scale RN32(amax / 448) equals
 // RN32(m / 448) * 2^e and the reciprocal RN32(1 / scale) equals
@@ -168,10 +155,12 @@ struct SliceQuant {
 // (an fma) is the correctly rounded quotient -- the division step of P.
 // Markstein, "Computation of elementary functions on the IBM RISC System/6000
 // processor", IBM J. Res. Develop. 34(1), 1990, which needs the reciprocal
-// correctly rounded and no intermediate to over- or underflow.  Groups whose
-// amax is below 2^-60 (their remainders could be subnormal) take the IEEE
-// division instead.  ue8m0 scales are powers of two, so there x * (1 / scale)
-// is the quotient itself.
+// correctly rounded and no intermediate to over- or underflow.  A group whose
+// amax is below 2^-60 is first multiplied by 2^64 (exact: the values are bf16,
+// far from the top of the range), its scale too, so no remainder that can
+// decide a code is subnormal; x / scale is unchanged.  (Quotients below
+// 2^-10 round to a zero code whatever their last bits.)  ue8m0 scales are
+// powers of two, so there x * (1 / scale) is the quotient itself.
 template <int KIND>
 __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __restrict__ tab) {
     float v[8];
@@ -198,36 +187,37 @@ __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __res
     }
     const uint32_t e_biased = amax_bits >> 23;
     float s, recip;
-    if (e_biased >= 10u) {
+    const bool normal_scale = e_biased >= 10u;
+    if (normal_scale) {
         const float2 t = tab[(amax_bits >> 16) & 0x7Fu];
         const int shift = (static_cast<int>(e_biased) - 127) * (1 << 23);
         s = __int_as_float(__float_as_int(t.x) + shift);
         recip = __int_as_float(__float_as_int(t.y) - shift);
-    } else {  // amax < 2^-117: scale and reciprocal leave the normal range
+    } else {  // amax < 2^-117: the scale is subnormal, its reciprocal set below
         s = __fdiv_rn(amax, 448.0f);
-        recip = __frcp_rn(s);
+        recip = 0.0f;
     }
+    float sx = s, rx = recip;  // the scale and reciprocal the quotients use
     if (KIND == FP8BS_SCALE_UE8M0) {
         out.byte = e8m0_ceil_byte(s);
         out.scale = e8m0_to_float(out.byte);
-        recip = e8m0_to_float(254u - out.byte);  // 2^(127 - e): exact
+        rx = e8m0_to_float(254u - out.byte);  // 2^(127 - e): exact
     } else {
         out.scale = s;
-    }
-    if (KIND == FP8BS_SCALE_F32 && !(amax >= 0x1p-60f)) {
-        // tiny groups: the IEEE quotients throughout
-        const uint2 c = e4m3_codes8_divide(raw, s);
-        out.lo = c.x;
-        out.hi = c.y;
-        return out;
+        if (!(amax >= 0x1p-60f)) {  // tiny group: work on x 2^64 (uniform per half-warp)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] *= 0x1p64f;  // exact; signs kept
+            sx = s * 0x1p64f;                              // exact, normal
+            rx = normal_scale ? recip * 0x1p-64f : __frcp_rn(sx);
+        }
     }
     float a[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        a[j] = v[j] * recip;
+        a[j] = v[j] * rx;
         // the correction gives +0 for x = -0 (0 + -0 rounds to +0): the
         // quotient keeps the sign of x, which copysign restores
-        if (KIND == FP8BS_SCALE_F32) a[j] = copysignf(fmaf(fmaf(-a[j], s, v[j]), recip, a[j]), v[j]);
+        if (KIND == FP8BS_SCALE_F32) a[j] = copysignf(fmaf(fmaf(-a[j], sx, v[j]), rx, a[j]), v[j]);
     }
     out.lo = e4m3x2(a[0], a[1]) | (e4m3x2(a[2], a[3]) << 16);
     out.hi = e4m3x2(a[4], a[5]) | (e4m3x2(a[6], a[7]) << 16);
