@@ -17,10 +17,10 @@
 // [c*T/G, (c+1)*T/G), at most 10-12.  Two CTAs fit on an SM (up to 32
 // tokens), so under programmatic dependent launch the next call's CTAs stream
 // their weights while this call's CTAs finish.
-//   1. Weight ring: one thread keeps 4-5 tiles in flight with bulk async
-//      copies (TMA, evict-first) and prefetches the CTA's other tiles into
-//      L2, all before the wait for the previous kernel; a slot is refilled as
-//      soon as the MMAs that read it complete.
+//   1. Weight ring: one thread puts the CTA's first 4-8 tiles in flight with
+//      bulk async copies (TMA, evict-first) and prefetches its other tiles
+//      into L2, before the wait for the previous kernel; a slot is refilled
+//      as soon as the MMAs that read it complete.
 //   2. Every CTA quantises the 1x128 groups of the K blocks its units touch
 //      (one "slot" per distinct K block, shared by units of equal K block),
 //      straight into the shared-memory B operands (K-major, 128-byte
@@ -29,10 +29,12 @@
 //      afterwards the instructions and parameters it uses are cached and only
 //      the x loads are cold.  With caller-quantised input the codes and
 //      scales are copied with cp.async instead.
-//   3. One thread issues the MMAs, the weight tile as the 128-row A operand
-//      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each:
-//        fp32 scales: four tcgen05.mma kind::f8f6f4 per unit into one of 4
-//        TMEM stages; four epilogue warps read each stage and accumulate
+//   3. One warp issues the MMAs, the weight tile as the 128-row A operand
+//      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each; a watcher
+//      warp waits for each unit's operands and tile and releases the issuer
+//      through a named barrier, so the issuer itself never probes an mbarrier:
+//        fp32 scales: four tcgen05.mma kind::f8f6f4 per unit into its own
+//        TMEM stage; four epilogue warps read each stage and accumulate
 //        P * (xs * ws) in fp32 registers (the page's per-K-block rescale);
 //        ue8m0 scales: kind::mxf8f6f4.block_scale MMAs whose per-32 scale
 //        factors sit in TMEM -- each 128-group scale replicated over its four
@@ -67,12 +69,11 @@ __device__ unsigned long long g_trace[kTraceCalls * kTraceCtas * kTracePoints * 
 #endif
 
 // 8 warps.  Warp 0: weight ring (one thread) and quant.  Warp 1: MMA issue
-// (one thread) and TMEM.  Warp 2: unit info and header check, then quant.
-// Warp 3: scale table, then quant.  Warps 4-7: quant, then the epilogue (one
-// warp per 32 TMEM lanes).
+// (one elected thread) and TMEM.  Warp 2: unit info and header check, then
+// quant.  Warp 3: scale table, then quant -- or, in the kernel that quantises
+// up to 16 tokens itself, the issue watcher.  Warps 4-7: quant, then the
+// epilogue (one warp per 32 TMEM lanes).
 constexpr int kThreads = 256;
-constexpr int kQuantHalfWarps = 14;  // warps 0 and 2-7
-constexpr int kQuantThreads = 16 * kQuantHalfWarps;
 constexpr int kQuantDepth = 4;       // groups per half-warp with their x loads in flight
 constexpr long long kSpinCycles = 4000;         // a wait probes without pause this long (~2 us) ...
 constexpr unsigned kBackoffNs = 128;            // ... then sleeps this long between probes
@@ -123,7 +124,9 @@ struct Cfg {
     static_assert(kBBytes % 1024 == 0, "operand tiles stay 1024-byte aligned");
     static_assert(kTmemUsed <= kTmemCols && kTmemCols * kCtasPerSm <= 512, "TMEM allocation");
     static_assert(kSfaCol % 4 == 0 && kSfbCol % 4 == 0, "scale-factor columns on 4-column boundaries");
-    static_assert(kStageFloats >= 2 * MPAD * 32 + 32 * ((kMaxCtas + 31) / 32), "gather stage");
+    static_assert(kStageFloats >= MPAD * 32, "gather stage");
+    static_assert(kUnits <= 15, "one named barrier (1..15) per unit");
+    static_assert(KIND == FP8BS_SCALE_UE8M0 || kAcc >= 4, "four stages probed at once");
 };
 
 struct Params {
@@ -257,8 +260,8 @@ __device__ __forceinline__ uint32_t slot_offset(uint32_t b, uint32_t c0, uint32_
 //             the stale words re-read until they carry the epoch) and sums
 //             each column in CTA order, its own partial at its place.
 // An owner's segment is always the last of its CTA's range, so the ring is
-// idle and its quarter q serves as the stage: the other contributors' slot
-// offsets, then its own values and the running sums of the owned columns.
+// idle and its quarter q serves as the stage for its own partials of the
+// owned columns.
 template <int MPAD>
 __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, const float (&acc)[MPAD], uint32_t c,
                                               uint32_t c0, uint32_t c1, uint32_t which0, int m_lo, int m_hi, int q,
@@ -285,22 +288,17 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     }
 #endif
     const int width = m_hi - m_lo;
-    uint32_t* tab = reinterpret_cast<uint32_t*>(stage);  // [owners] other contributors' slot offsets
-    float* own = stage + (owners + 31) / 32 * 32;       // [width][32]
-    float* sum = own + width * 32;                      // [width][32]
-#pragma unroll 1
-    for (int j = lane; j < owners; j += 32) {
-        const uint32_t b = c0 + static_cast<uint32_t>(j) + (c0 + static_cast<uint32_t>(j) >= c ? 1u : 0u);
-        tab[j] = slot_offset(b, c0, which0) + static_cast<uint32_t>(m_lo * kTile);
-    }
+    float* own = stage;  // [width][32]: this CTA's partials of the owned columns
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
-        if (m >= m_lo && m < m_hi) {
-            own[(m - m_lo) * 32 + lane] = acc[m];
-            sum[(m - m_lo) * 32 + lane] = 0.0f;
-        }
+        if (m >= m_lo && m < m_hi) own[(m - m_lo) * 32 + lane] = acc[m];
     __syncwarp();
-    // word t = j * width + col: column m_lo + col of the j-th other contributor
+    // word t = col * owners + j: column m_lo + col of the j-th other contributor,
+    // b = c0 + j, or c0 + j + 1 from this CTA on.  Addresses come from
+    // registers (no table in shared memory between the loads), and each
+    // column is summed in a register as its words arrive, in CTA order, then
+    // stored.
+    const uint64_t* col0 = p.slots + static_cast<uint32_t>(m_lo * kTile + r);
     const int nw = owners * width;
     constexpr int kRound = 16;
     bool ok = true;
@@ -310,19 +308,23 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         FP8BS_STAMP_CLK(rec, kTpEpoch);  // the gather's set-up done, its loads about to go out
     }
 #endif
-#pragma unroll 1
     int jr = 0, colr = 0;  // word `base` = column colr of the jr-th other contributor
+    float run = 0.0f;      // the running sum of column colr
+#pragma unroll 1
     for (int base = 0; base < nw && ok; base += kRound) {
-        uint32_t off[kRound];
+        // word k of the round: its offset from col0 (recomputed for a re-read)
+        const auto word_off = [&](int jj, int cc) {
+            const uint32_t b = c0 + static_cast<uint32_t>(jj) + (static_cast<int>(c0) + jj >= static_cast<int>(c) ? 1u : 0u);
+            return slot_offset(b, c0, which0) + static_cast<uint32_t>(cc * kTile);
+        };
         uint64_t w[kRound];
         int j = jr, col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
-            off[k] = base + k < nw ? tab[j] + static_cast<uint32_t>(col * kTile + r) : 0u;
-            w[k] = base + k < nw ? ld_word(p.slots + off[k]) : tag(0, epoch);
-            if (++col == width) {
-                col = 0;
-                ++j;
+            w[k] = base + k < nw ? ld_word(col0 + word_off(j, col)) : tag(0, epoch);
+            if (++j == owners) {
+                j = 0;
+                ++col;
             }
         }
         const long long t0 = clock64();
@@ -354,24 +356,36 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
                 ok = false;
                 break;
             }
+            j = jr;
+            col = colr;
 #pragma unroll
-            for (int k = 0; k < kRound; ++k)
-                if (!tagged(w[k], epoch)) w[k] = ld_word(p.slots + off[k]);
+            for (int k = 0; k < kRound; ++k) {
+                if (!tagged(w[k], epoch)) w[k] = ld_word(col0 + word_off(j, col));
+                if (++j == owners) {
+                    j = 0;
+                    ++col;
+                }
+            }
         }
-        // running sums in CTA order: the own partial enters just before the
-        // first other contributor that follows this CTA (j == s)
+        if (!ok) break;
+        // the sums in CTA order: the own partial enters just before the first
+        // other contributor that follows this CTA (j == s); a column is
+        // stored as soon as its last word is in
         j = jr;
         col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
             if (base + k < nw) {
-                float v = sum[col * 32 + lane];
-                if (j == s) v += own[col * 32 + lane];
-                sum[col * 32 + lane] = v + __uint_as_float(static_cast<uint32_t>(w[k]));
+                if (j == s) run += own[col * 32 + lane];
+                run += __uint_as_float(static_cast<uint32_t>(w[k]));
+                if (j + 1 == owners) {
+                    yrow[(m_lo + col) * p.ldy] = f32_to_bf16_rn(run);
+                    run = 0.0f;
+                }
             }
-            if (++col == width) {
-                col = 0;
-                ++j;
+            if (++j == owners) {
+                j = 0;
+                ++col;
             }
         }
         jr = j;  // the next round starts where this one ended
@@ -384,8 +398,6 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         FP8BS_STAMP_CLK(rec, kTpGatherSummed);
     }
 #endif
-#pragma unroll 1
-    for (int col = 0; col < width; ++col) yrow[(m_lo + col) * p.ldy] = f32_to_bf16_rn(sum[col * 32 + lane]);
     return true;
 }
 
@@ -478,8 +490,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                           &full[i], pol);
         }
         misc[kMiscIssued] = static_cast<uint32_t>(pre);
-        // (no L2 prefetch of the tiles beyond the ring: measured not to pay, a
-        // bulk prefetch sits in the SM's memory queue ahead of later loads)
+        // the tiles beyond the ring into L2 (one bulk prefetch: they are
+        // contiguous), so that their refills, issued in one burst by every
+        // CTA as its first MMAs complete, come from L2 rather than DRAM
+        if (cnt > pre)
+            ptx::bulk_prefetch_l2(p.tiles + static_cast<size_t>(u0 + pre) * kTileBytes,
+                                  static_cast<uint32_t>(cnt - pre) * kTileBytes);
     }
 
     if (warp == 1) {
@@ -533,8 +549,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         }
         ptx::tmem_wait_st();
     }
-    const bool quant_warp = warp != 1;
-    const int qt = warp == 0 ? tid : tid - 32;  // quantising threads 0..223
+    // the issue watcher (warp 3) where it was measured to pay: 16-token tiles
+    // quantised here (with 32 the quant is the longer phase and needs warp 3)
+    constexpr bool kWatch = MPAD == 16 && SRC == kSrcQuant;
+    constexpr int kQuantHalfWarps = kWatch ? 12 : 14;  // warps 0, 2 (3) and 4-7
+    constexpr int kQuantThreads = 16 * kQuantHalfWarps;
+    const bool quant_warp = warp != 1 && !(kWatch && warp == 3);
+    const int qt = warp == 0 ? tid : (kWatch && warp >= 4 ? tid - 64 : tid - 32);  // quantising threads
     const int hw = qt >> 4;
     const int l16 = qt & 15;
     const int hw_first = hw & ~1;  // the warp's first half-warp
@@ -555,7 +576,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
     if (SRC == kSrcQuant && quant_warp) {
         // ---- 2. quantise the groups of this CTA's K-block slots -------------------
         // group g = slot * M + m (slot-major, so slot 0 is ready first); the
-        // half-warp's t-th group is g = hw + 14 t, in rounds of kQuantDepth:
+        // half-warp's t-th group is g = hw + H t (H = kQuantHalfWarps), in
+        // rounds of kQuantDepth:
         // a round first issues the x loads of the next round, then quantises
         // its own groups, so one round of work covers the load latency.  Pass
         // 0 runs one round of this code on dummy values before the wait,
@@ -598,11 +620,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                         nxt[k] = ptx::ld_global_v4(p.x + m2 * p.ldx + kb2 * kTile + l16 * 8);
                     }
                 }
+                // every slot of the round, valid or not (straight-line code, so
+                // the groups interleave); a rare group is then redone exactly
+                // (a round whose warp holds a single group computes only that one)
                 SliceQuant qs[kQuantDepth];
+                bool rare[kQuantDepth];
+                if (pass == 1 && hw_first + kQuantHalfWarps * (t0 + 1) >= ng) {  // warp-uniform
+                    qs[0] = quant_slice_fast<KIND>(raw[0], sTab, rare[0]);
+#pragma unroll
+                    for (int k = 1; k < kQuantDepth; ++k) {
+                        qs[k] = qs[0];
+                        rare[k] = false;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kQuantDepth; ++k) qs[k] = quant_slice_fast<KIND>(raw[k], sTab, rare[k]);
+                }
 #pragma unroll
                 for (int k = 0; k < kQuantDepth; ++k) {
-                    qs[k].lo = qs[k].hi = 0;
-                    if (pass == 0 || hw_first + kQuantHalfWarps * (t0 + k) < ng) qs[k] = quant_slice<KIND>(raw[k], sTab);  // warp-uniform
+                    if (__any_sync(0xFFFFFFFFu, rare[k])) {
+                        const SliceQuant r = quant_slice<KIND>(raw[k], sTab);
+                        if (rare[k]) qs[k] = r;
+                    }
                     sink ^= qs[k].lo;
                 }
                 if (pass == 1) {
@@ -704,27 +743,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         __syncwarp();
     } else if (warp == 1) {
         // ---- 3. MMA issue ----------------------------------------------------------
-        // The whole warp runs this loop, with warp-uniform values (lane 0 polls,
-        // a shuffle hands the answer to the warp), and one elected lane issues
-        // each MMA and commit: measured to issue units about twice as fast as
-        // the same loop run by lane 0 alone.  An mbarrier probe takes ~180
-        // cycles to answer, so the issuer probes in batches: the ring's first
-        // tiles (requested long before) once at the start, and the K-block
-        // operands four at a time; it waits on one barrier only when a batch
-        // says not yet.  The accumulator stages outnumber the units of most
-        // CTAs, so waits for the epilogue are rare.
-        bool ok = !kBlockScaled || warp_wait_bar(sf_bar, 0, p, misc, lane);
+        // The whole warp runs this loop, with warp-uniform values, and one
+        // elected lane issues each MMA and commit (measured to issue units
+        // about twice as fast as the same loop run by lane 0 alone).  With
+        // the watcher, unit i waits only on named barrier 1 + i, which warp 3
+        // passes once the unit's operands, ring tile and accumulator stage
+        // are ready: an mbarrier probe from this warp queues behind the
+        // MMAs' shared-memory operand reads (~250 cycles each, measured), a
+        // named barrier does not.  Without it the warp probes for itself, in
+        // batches: the ring's first tiles once at the start, the K-block
+        // operands four at a time, and waits on one barrier only when a batch
+        // says not yet.  Nothing is stored to shared memory inside the loop
+        // (a generic store waits behind those reads too); the count of
+        // committed units is stored once, after it.
+        bool ok = kWatch || !kBlockScaled || warp_wait_bar(sf_bar, 0, p, misc, lane);
         uint32_t known = 0;  // bit s: ring slot s holds its first tile; bit 16 + j: slot j's operand is ready
-        if (lane == 0)
-            for (int s0 = 0; s0 < S && s0 < cnt; s0 += 4)
-                known |= ptx::mbar_test4(&full[s0], 0, &full[(s0 + 1) % S], 0, &full[(s0 + 2) % S], 0,
-                                         &full[(s0 + 3) % S], 0) << s0;
-        known = __shfl_sync(0xFFFFFFFFu, known, 0);
+        if (!kWatch) {
+            if (lane == 0)
+                for (int s0 = 0; s0 < S && s0 < cnt; s0 += 4)
+                    known |= ptx::mbar_test4(&full[s0], 0, &full[(s0 + 1) % S], 0, &full[(s0 + 2) % S], 0,
+                                             &full[(s0 + 3) % S], 0) << s0;
+            known = __shfl_sync(0xFFFFFFFFu, known, 0);
+        }
         uint32_t seg = 0, kb = kb0;  // tile segment of unit i and its K block
         int islot = 0;               // unit i's K-block slot, i % KB
-        // nothing is stored to shared memory inside this loop: a generic
-        // store queued behind the MMAs' operand reads was measured to hold
-        // the thread; the count of committed units is stored once, after it
         int committed = 0;
 #ifdef FP8BS_TRACE
         long long cyc[5] = {0, 0, 0, 0, 0}, t_prev = clock64();
@@ -744,29 +786,34 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
             const int slot = islot;  // i % KB, kept by increments (no division in this loop)
             const bool seg_start = i == 0 || kb == 0;
             const int a = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) % NA);
-            const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
-            if (!kBlockScaled && !((known >> (16 + slot)) & 1u)) {
-                const int j = slot;  // probe this slot and the next three
-                uint32_t got = 0;
-                if (lane == 0)
-                    got = ptx::mbar_test4(&bready[j], 0, &bready[j + 1 < nslots ? j + 1 : j], 0,
-                                          &bready[j + 2 < nslots ? j + 2 : j], 0, &bready[j + 3 < nslots ? j + 3 : j], 0);
-                known |= __shfl_sync(0xFFFFFFFFu, got, 0) << (16 + j);
-                if (!((known >> (16 + slot)) & 1u)) {
-                    if (!warp_wait_bar(&bready[slot], 0, p, misc, lane)) break;
-                    known |= 1u << (16 + slot);
+            if constexpr (kWatch) {
+                ptx::named_sync(1u + static_cast<uint32_t>(i), 64u);
+                FP8BS_ISS_LAP(0);
+            } else {
+                const int use = static_cast<int>((kBlockScaled ? seg : static_cast<uint32_t>(i)) / NA);
+                if (!kBlockScaled && !((known >> (16 + slot)) & 1u)) {
+                    const int j = slot;  // probe this slot and the next three
+                    uint32_t got = 0;
+                    if (lane == 0)
+                        got = ptx::mbar_test4(&bready[j], 0, &bready[j + 1 < nslots ? j + 1 : j], 0,
+                                              &bready[j + 2 < nslots ? j + 2 : j], 0,
+                                              &bready[j + 3 < nslots ? j + 3 : j], 0);
+                    known |= __shfl_sync(0xFFFFFFFFu, got, 0) << (16 + j);
+                    if (!((known >> (16 + slot)) & 1u)) {
+                        if (!warp_wait_bar(&bready[slot], 0, p, misc, lane)) break;
+                        known |= 1u << (16 + slot);
+                    }
                 }
+                FP8BS_ISS_LAP(0);
+                if (!(i < S && ((known >> i) & 1u)) &&
+                    !warp_wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc, lane))
+                    break;
+                FP8BS_ISS_LAP(1);
+                if ((seg_start || !kBlockScaled) && use > 0 &&
+                    !warp_wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc, lane))
+                    break;
+                FP8BS_ISS_LAP(2);
             }
-            FP8BS_ISS_LAP(0);
-            if (!(i < S && ((known >> i) & 1u)) &&
-                !warp_wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc, lane))
-                break;
-            FP8BS_ISS_LAP(1);
-            if ((seg_start || !kBlockScaled) && use > 0 &&
-                !warp_wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc, lane))
-                break;
-            FP8BS_ISS_LAP(2);
-
             ptx::tc_fence_after();
             const uint32_t wa = ptx::smem_addr(sRing + s * kTileBytes);
             const uint32_t xb = ptx::smem_addr(sB + slot * C::kBBytes);
@@ -813,6 +860,67 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         }
 #endif
         __syncwarp();
+    } else if (kWatch && warp == 3) {
+        // ---- 3'. the issue watcher ---------------------------------------------------
+        // Releases unit i to the issuer (named barrier 1 + i: each id serves
+        // one unit, so no barrier is reused within a launch) once its K-block
+        // operand (fp32 scales; ue8m0: the token scale factors in TMEM, which
+        // follow every operand), its ring tile and its accumulator stage are
+        // ready.  Operands and tiles are probed four at a time, ahead of the
+        // unit; it waits on one barrier only when a probe says not yet.  A
+        // probe of a tile four units on is sound: with a ring of at least four
+        // slots, that slot's previous phase is one this warp already saw
+        // complete.  After a failed wait it releases the remaining units
+        // without waiting (their MMAs read stale operands; the call reports
+        // the error), so the issuer never waits on a barrier nobody passes.
+        bool ok = !kBlockScaled || warp_wait_bar(sf_bar, 0, p, misc, lane);
+        uint32_t seg = 0, kb = kb0;
+        int islot = 0;
+        uint32_t op_known = 0, tile_known = 0;  // bit j: slot j's operand / unit j's tile is ready
+#pragma unroll 1
+        for (int i = 0; i < cnt; ++i) {
+            const int s = i % S;
+            const int slot = islot;
+            const bool seg_start = i == 0 || kb == 0;
+            const uint32_t su = kBlockScaled ? seg : static_cast<uint32_t>(i);
+            const int a = static_cast<int>(su % NA), use = static_cast<int>(su / NA);
+            if (ok && !kBlockScaled && !((op_known >> slot) & 1u)) {
+                uint32_t got = 0;
+                if (lane == 0) {
+                    const int j1 = slot + 1 < nslots ? slot + 1 : slot, j2 = slot + 2 < nslots ? slot + 2 : slot;
+                    const int j3 = slot + 3 < nslots ? slot + 3 : slot;
+                    got = ptx::mbar_test4(&bready[slot], 0, &bready[j1], 0, &bready[j2], 0, &bready[j3], 0);
+                }
+                op_known |= __shfl_sync(0xFFFFFFFFu, got, 0) << slot;
+                if (!((op_known >> slot) & 1u)) {
+                    ok = warp_wait_bar(&bready[slot], 0, p, misc, lane);
+                    op_known |= 1u << slot;
+                }
+            }
+            if (ok && !((tile_known >> i) & 1u)) {
+                uint32_t got = 0;
+                if (lane == 0) {
+                    const int i1 = i + 1 < cnt ? i + 1 : i, i2 = i + 2 < cnt ? i + 2 : i, i3 = i + 3 < cnt ? i + 3 : i;
+                    got = ptx::mbar_test4(&full[s], static_cast<uint32_t>((i / S) & 1), &full[i1 % S],
+                                          static_cast<uint32_t>((i1 / S) & 1), &full[i2 % S],
+                                          static_cast<uint32_t>((i2 / S) & 1), &full[i3 % S],
+                                          static_cast<uint32_t>((i3 / S) & 1));
+                }
+                tile_known |= __shfl_sync(0xFFFFFFFFu, got, 0) << i;
+                if (!((tile_known >> i) & 1u)) {
+                    ok = warp_wait_bar(&full[s], static_cast<uint32_t>((i / S) & 1), p, misc, lane);
+                    tile_known |= 1u << i;
+                }
+            }
+            if (ok && (seg_start || !kBlockScaled) && use > 0)
+                ok = warp_wait_bar(&acce[a], static_cast<uint32_t>((use - 1) & 1), p, misc, lane);
+            ptx::named_arrive(1u + static_cast<uint32_t>(i), 64u);
+            if (++islot == p.KB) islot = 0;
+            if (++kb == KB || i == cnt - 1) {
+                kb = 0;
+                ++seg;
+            }
+        }
     }
 
     if (warp >= 4) {
@@ -855,38 +963,56 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 for (; i < ib; ++i) {
                     const int a = i % NA;
                     if (i >= seen) {
-                        // units complete in order: one probe of the unit three
-                        // on may cover four; else wait for this one
-                        const int j = i + 3 < cnt ? i + 3 : cnt - 1;
+                        // units complete in order: one probe of units i..i+3
+                        // (their latencies overlap) tells how many are done;
+                        // if unit i is not, wait for it.  Each of these
+                        // stages' previous use is already seen complete
+                        // (stages >= 8), so the parity tests are sound.
                         uint32_t got = 0;
-                        if (lane == 0) got = ptx::mbar_test(&accfull[j % NA], static_cast<uint32_t>((j / NA) & 1)) ? 1u : 0u;
-                        if (__shfl_sync(0xFFFFFFFFu, got, 0) != 0) {
-                            seen = j + 1;
-                        } else {
+                        if (lane == 0) {
+                            const int j1 = i + 1 < cnt ? i + 1 : i, j2 = i + 2 < cnt ? i + 2 : i, j3 = i + 3 < cnt ? i + 3 : i;
+                            got = ptx::mbar_test4(&accfull[a], static_cast<uint32_t>((i / NA) & 1), &accfull[j1 % NA],
+                                                  static_cast<uint32_t>((j1 / NA) & 1), &accfull[j2 % NA],
+                                                  static_cast<uint32_t>((j2 / NA) & 1), &accfull[j3 % NA],
+                                                  static_cast<uint32_t>((j3 / NA) & 1));
+                        }
+                        const int n = __ffs(~__shfl_sync(0xFFFFFFFFu, got, 0)) - 1;  // leading units done
+                        if (n == 0) {
                             ok = warp_wait_bar(&accfull[a], static_cast<uint32_t>((i / NA) & 1), p, misc, lane);
                             if (!ok) break;
                             seen = i + 1;
+                        } else {
+                            seen = i + n < cnt ? i + n : cnt;
                         }
                     }
                     ptx::tc_fence_after();
                     if (i < 8 && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiSeen + i);
                     const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * MPAD);
                     const float sw = sWs[i];
-                    const uint32_t* xs = sXs + xslot * MPAD;
+                    const uint4* xs4 = reinterpret_cast<const uint4*>(sXs + xslot * MPAD);  // 64-byte aligned
                     if (++xslot == p.KB) xslot = 0;
 #pragma unroll
                     for (int h = 0; h < MPAD / 16; ++h) {
                         uint32_t rr[16];
                         ptx::tmem_ld_32x32b_x16(taddr + 16 * h, rr);
+                        uint32_t xs[16];
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 t = xs4[4 * h + v];
+                            xs[4 * v] = t.x;
+                            xs[4 * v + 1] = t.y;
+                            xs[4 * v + 2] = t.z;
+                            xs[4 * v + 3] = t.w;
+                        }
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            acc[16 * h + m] =
-                                fmaf(__uint_as_float(rr[m]), __uint_as_float(xs[16 * h + m]) * sw, acc[16 * h + m]);
+                            acc[16 * h + m] = fmaf(__uint_as_float(rr[m]), __uint_as_float(xs[m]) * sw, acc[16 * h + m]);
                     }
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&acce[a]);
+                    // the stage is released only if a later unit of this CTA takes it
+                    if (lane == 0 && i + NA < cnt) ptx::mbar_arrive(&acce[a]);
                     if (i < 10 && tid == 128) FP8BS_STAMP_CLK(trec, kTpEpiUnit + i);
                 }
                 if (!ok) break;

@@ -224,6 +224,54 @@ __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __res
     return out;
 }
 
+// The common case of quant_slice without a branch, for callers that quantise
+// several groups at once: exact (the same codes and scale as quant_slice) for
+// a group whose amax is at least 2^-60, where the scale is normal, its
+// reciprocal comes from the table and no rescaling is needed.  rare is set for
+// every other group (zero, tiny, subnormal scale, or NaN amax): the caller
+// takes that group's result from quant_slice instead.  Being straight-line
+// code, the calls for independent groups interleave.  All 32 lanes call it.
+template <int KIND>
+__device__ __forceinline__ SliceQuant quant_slice_fast(uint4 raw, const float2* __restrict__ tab, bool& rare) {
+    float v[8];
+    unpack_bf16x8(raw, v);
+    const float m0 = fmaxf(fabsf(v[0]), fabsf(v[1])), m1 = fmaxf(fabsf(v[2]), fabsf(v[3]));
+    const float m2 = fmaxf(fabsf(v[4]), fabsf(v[5])), m3 = fmaxf(fabsf(v[6]), fabsf(v[7]));
+    const uint32_t mine = __float_as_uint(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+    const bool low_half = (threadIdx.x & 31u) < 16u;
+    const uint32_t g0 = __reduce_max_sync(0xFFFFFFFFu, low_half ? mine : 0u);
+    const uint32_t g1 = __reduce_max_sync(0xFFFFFFFFu, low_half ? 0u : mine);
+    const uint32_t amax_bits = low_half ? g0 : g1;
+    rare = !(__uint_as_float(amax_bits) >= 0x1p-60f);
+    // scale and reciprocal from the table, shifted by the exponent of amax
+    // (unsigned arithmetic: a rare group's values are discarded)
+    const float2 t = tab[(amax_bits >> 16) & 0x7Fu];
+    const uint32_t shift = ((amax_bits >> 23) - 127u) << 23;
+    const float s = __uint_as_float(__float_as_uint(t.x) + shift);
+    float rx = __uint_as_float(__float_as_uint(t.y) - shift);
+    SliceQuant out;
+    if (KIND == FP8BS_SCALE_UE8M0) {
+        // the smallest power of two >= s, s normal: its e8m0 byte, clamped
+        const uint32_t b = __float_as_uint(s);
+        const uint32_t byte = min((b >> 23) + ((b & 0x7FFFFFu) != 0u ? 1u : 0u), 254u);
+        out.byte = byte;
+        out.scale = __uint_as_float(byte << 23);
+        rx = __uint_as_float(byte == 254u ? 0x00400000u : (254u - byte) << 23);  // 2^(127 - e): exact
+    } else {
+        out.byte = 0;
+        out.scale = s;
+    }
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a[j] = v[j] * rx;
+        if (KIND == FP8BS_SCALE_F32) a[j] = copysignf(fmaf(fmaf(-a[j], s, v[j]), rx, a[j]), v[j]);
+    }
+    out.lo = e4m3x2(a[0], a[1]) | (e4m3x2(a[2], a[3]) << 16);
+    out.hi = e4m3x2(a[4], a[5]) | (e4m3x2(a[6], a[7]) << 16);
+    return out;
+}
+
 // ---------------------------------------------------------------------------
 // Launchers (argument checks are done by the C ABI before these run)
 // ---------------------------------------------------------------------------

@@ -233,6 +233,15 @@ __device__ __forceinline__ void mma_mxf8f6f4_bs_warp(uint32_t d_tmem, uint64_t a
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
 }
+// Named (hardware) barriers: bar.arrive marks the arrival of the calling warp
+// without waiting; bar.sync waits until `count` threads have arrived.
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"

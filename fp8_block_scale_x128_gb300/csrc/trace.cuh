@@ -44,10 +44,11 @@ enum TracePoint : int {
     kTpMmaIssued = 44,  // + i (i < 4): the MMA issuer, unit i's commits issued
     kTpEpiSeen = 48,    // + i (i < 8): epilogue warp 0, unit i's sum known complete (fp32 scales)
     kTpIssCycles = 56,  // + j (j < 5): the MMA issuer's cycles summed over its loop, in the clock field:
-                        // waiting for operands, for ring tiles, for accumulator stages, issuing, the rest
+                        // waiting for operands (or the watcher's release), for ring tiles, for
+                        // accumulator stages, issuing, the rest
     kTpGatherLoaded = 61,  // epilogue warp 0, an owner's first round of partial words back (tagged or not)
     kTpGatherPolls = 62,   // epilogue warp 0, an owner's re-polls summed over its rounds (count, clock field)
-    kTpGatherSummed = 63,  // epilogue warp 0, an owner's sums done (before the y stores)
+    kTpGatherSummed = 63,  // epilogue warp 0, an owner's columns summed and stored
     kTpCount = 64,
 };
 

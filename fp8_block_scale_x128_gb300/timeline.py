@@ -35,13 +35,13 @@ POINTS = (["entry", "setup", "wait", "quant_first", "quant_done", "xchg_done", "
            "gather"] + [f"mma_unit{i}" for i in range(10)] + [f"epi_unit{i}" for i in range(10)]
           + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)]
           + [f"epi_seen{i}" for i in range(8)]
-          + ["iss_operand", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
+          + ["iss_wait", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
           + ["gather_loaded", "gather_polls", "gather_summed"])
 # points that hold a count, not a time
 COUNTS = ["gather_polls"]
 # points that hold a cycle count (a duration), not a time
-DURATIONS = ["iss_operand", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
-PHASES = (["xload", "xchg_done", "mma_first", "mma_issued0", "mma_issued1", "quant_first", "quant_done", "mma_last",
+DURATIONS = ["iss_wait", "iss_ring", "iss_acc", "iss_issue", "iss_rest"]
+PHASES = (["xload", "xchg_done", "quant_first", "quant_done", "mma_last",
            "epi_last", "publish", "gather", "epoch", "gather_loaded", "gather_summed", "reduce_end", "teardown", "exit"]
           + [f"mma_unit{i}" for i in range(10)] + [f"epi_unit{i}" for i in range(10)]
           + [f"refill{j}" for j in range(8)] + [f"mma_issued{i}" for i in range(4)]
