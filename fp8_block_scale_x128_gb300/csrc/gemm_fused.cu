@@ -176,25 +176,34 @@ __device__ __forceinline__ uint32_t cta_of(uint32_t u, uint32_t T, uint32_t G) {
 
 __device__ __forceinline__ uint32_t div_m(uint32_t g, uint64_t mdiv) { return static_cast<uint32_t>((g * mdiv) >> 32); }
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
-    uint16_t r;
-    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
-    return r;
-}
-
 __device__ __forceinline__ uint64_t tag(uint32_t data, uint32_t epoch) {
     return static_cast<uint64_t>(data) | (static_cast<uint64_t>(epoch) << 32);
 }
 __device__ __forceinline__ bool tagged(uint64_t w, uint32_t epoch) { return static_cast<uint32_t>(w >> 32) == epoch; }
 
-// Single-copy-atomic 64-bit exchange words (relaxed, GPU scope).
-__device__ __forceinline__ void st_word(uint64_t* p, uint64_t a) {
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(a) : "memory");
+// Accesses to the partial words (single-copy-atomic 64-bit, relaxed, gpu
+// scope) and to y (bf16, rounded to nearest even), done only
+// where pred holds, with the predicate inside the instruction: a branch
+// around an asm statement (which the compiler cannot predicate) costs a
+// divergence-safe branch per word, and the unrolled gather loops were
+// measured several times slower with them.  ld_word_if leaves w unchanged
+// where pred is false.
+__device__ __forceinline__ void st_word_if(uint64_t* p, uint64_t a, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.relaxed.gpu.global.b64 [%0], %1;\n\t}" ::"l"(p),
+                 "l"(a), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
 }
-__device__ __forceinline__ uint64_t ld_word(const uint64_t* p) {
-    uint64_t a;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
-    return a;
+__device__ __forceinline__ void ld_word_if(uint64_t& w, const uint64_t* p, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q ld.relaxed.gpu.global.b64 %0, [%1];\n\t}"
+                 : "+l"(w)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+__device__ __forceinline__ void st_bf16_if(uint16_t* p, float v, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\t.reg .b16 h;\n\tsetp.ne.u32 q, %2, 0;\n\tcvt.rn.bf16.f32 h, %1;\n\t"
+                 "@q st.global.b16 [%0], h;\n\t}" ::"l"(p),
+                 "f"(v), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
 }
 
 // Cold path of every bounded wait.
@@ -270,8 +279,7 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     uint16_t* yrow = p.y + static_cast<size_t>(nt) * kTile + r;
     if (c0 == c1) {
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m)
-            if (m < p.M) yrow[m * p.ldy] = f32_to_bf16_rn(acc[m]);
+        for (int m = 0; m < MPAD; ++m) st_bf16_if(yrow + m * p.ldy, acc[m], m < p.M);
         return true;
     }
     const int owners = static_cast<int>(c1 - c0);
@@ -279,7 +287,7 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     uint64_t* mine = p.slots + slot_offset(c, c0, which0) + r;
 #pragma unroll
     for (int m = 0; m < MPAD; ++m)
-        if (m < p.M && (m < m_lo || m >= m_hi)) st_word(mine + m * kTile, tag(__float_as_uint(acc[m]), epoch));
+        st_word_if(mine + m * kTile, tag(__float_as_uint(acc[m]), epoch), m < p.M && (m < m_lo || m >= m_hi));
     if (m_lo == m_hi) return true;
 #ifdef FP8BS_TRACE
     if (q == 0 && lane == 0) {
@@ -300,14 +308,19 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
     // stored.
     const uint64_t* col0 = p.slots + static_cast<uint32_t>(m_lo * kTile + r);
     const int nw = owners * width;
-    constexpr int kRound = 16;
-    bool ok = true;
 #ifdef FP8BS_TRACE
     if (q == 0 && lane == 0) {
         volatile unsigned long long* rec = reinterpret_cast<volatile unsigned long long*>(misc + 16);
         FP8BS_STAMP_CLK(rec, kTpEpoch);  // the gather's set-up done, its loads about to go out
     }
 #endif
+    // rounds of 16 words per lane in flight.  With 16 tokens an owner often
+    // has only a few words (3-4 at one token): a round then stops at the first
+    // group of four past its last word (one uniform branch per group, kept
+    // where measured to pay; with 32 or more tokens the words fill the round)
+    constexpr int kRound = 16;
+    constexpr bool kSkip = MPAD == 16;
+    bool ok = true;
     int jr = 0, colr = 0;  // word `base` = column colr of the jr-th other contributor
     float run = 0.0f;      // the running sum of column colr
 #pragma unroll 1
@@ -317,15 +330,19 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
             const uint32_t b = c0 + static_cast<uint32_t>(jj) + (static_cast<int>(c0) + jj >= static_cast<int>(c) ? 1u : 0u);
             return slot_offset(b, c0, which0) + static_cast<uint32_t>(cc * kTile);
         };
+        // straight-line code throughout (selects and predicated accesses, no
+        // branch per word)
         uint64_t w[kRound];
         int j = jr, col = colr;
 #pragma unroll
+        for (int k = 0; k < kRound; ++k) w[k] = tag(0, epoch);
+#pragma unroll
         for (int k = 0; k < kRound; ++k) {
-            w[k] = base + k < nw ? ld_word(col0 + word_off(j, col)) : tag(0, epoch);
-            if (++j == owners) {
-                j = 0;
-                ++col;
-            }
+            if (kSkip && k % 4 == 0 && base + k >= nw) break;
+            ld_word_if(w[k], col0 + word_off(j, col), base + k < nw);
+            const bool wrap = j + 1 == owners;
+            j = wrap ? 0 : j + 1;
+            col = wrap ? col + 1 : col;
         }
         const long long t0 = clock64();
 #ifdef FP8BS_TRACE
@@ -360,11 +377,11 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
             col = colr;
 #pragma unroll
             for (int k = 0; k < kRound; ++k) {
-                if (!tagged(w[k], epoch)) w[k] = ld_word(col0 + word_off(j, col));
-                if (++j == owners) {
-                    j = 0;
-                    ++col;
-                }
+                if (kSkip && k % 4 == 0 && base + k >= nw) break;
+                ld_word_if(w[k], col0 + word_off(j, col), !tagged(w[k], epoch));
+                const bool wrap = j + 1 == owners;
+                j = wrap ? 0 : j + 1;
+                col = wrap ? col + 1 : col;
             }
         }
         if (!ok) break;
@@ -375,18 +392,15 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
-            if (base + k < nw) {
-                if (j == s) run += own[col * 32 + lane];
-                run += __uint_as_float(static_cast<uint32_t>(w[k]));
-                if (j + 1 == owners) {
-                    yrow[(m_lo + col) * p.ldy] = f32_to_bf16_rn(run);
-                    run = 0.0f;
-                }
-            }
-            if (++j == owners) {
-                j = 0;
-                ++col;
-            }
+            if (kSkip && k % 4 == 0 && base + k >= nw) break;
+            const bool valid = base + k < nw, wrap = j + 1 == owners;
+            const float ov = own[(col < width ? col : width - 1) * 32 + lane];
+            run = valid && j == s ? run + ov : run;
+            run = valid ? run + __uint_as_float(static_cast<uint32_t>(w[k])) : run;
+            st_bf16_if(yrow + (m_lo + col) * p.ldy, run, valid && wrap);
+            run = valid && wrap ? 0.0f : run;
+            j = wrap ? 0 : j + 1;
+            col = wrap ? col + 1 : col;
         }
         jr = j;  // the next round starts where this one ended
         colr = col;
@@ -963,20 +977,30 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 for (; i < ib; ++i) {
                     const int a = i % NA;
                     if (i >= seen) {
-                        // units complete in order: one probe of units i..i+3
-                        // (their latencies overlap) tells how many are done;
-                        // if unit i is not, wait for it.  Each of these
-                        // stages' previous use is already seen complete
-                        // (stages >= 8), so the parity tests are sound.
+                        // units complete in order.  16 tokens: one probe of
+                        // units i..i+3 (their latencies overlap) tells how many
+                        // are done; each of these stages' previous use is
+                        // already seen complete (stages >= 8), so the parity
+                        // tests are sound.  32 or 64: one probe of unit i+3
+                        // covers four or none (measured the faster choice at
+                        // each width).  If unit i is not done, wait for it.
                         uint32_t got = 0;
-                        if (lane == 0) {
-                            const int j1 = i + 1 < cnt ? i + 1 : i, j2 = i + 2 < cnt ? i + 2 : i, j3 = i + 3 < cnt ? i + 3 : i;
-                            got = ptx::mbar_test4(&accfull[a], static_cast<uint32_t>((i / NA) & 1), &accfull[j1 % NA],
-                                                  static_cast<uint32_t>((j1 / NA) & 1), &accfull[j2 % NA],
-                                                  static_cast<uint32_t>((j2 / NA) & 1), &accfull[j3 % NA],
-                                                  static_cast<uint32_t>((j3 / NA) & 1));
+                        int n;
+                        if constexpr (MPAD == 16) {
+                            if (lane == 0) {
+                                const int j1 = i + 1 < cnt ? i + 1 : i, j2 = i + 2 < cnt ? i + 2 : i;
+                                const int j3 = i + 3 < cnt ? i + 3 : i;
+                                got = ptx::mbar_test4(&accfull[a], static_cast<uint32_t>((i / NA) & 1), &accfull[j1 % NA],
+                                                      static_cast<uint32_t>((j1 / NA) & 1), &accfull[j2 % NA],
+                                                      static_cast<uint32_t>((j2 / NA) & 1), &accfull[j3 % NA],
+                                                      static_cast<uint32_t>((j3 / NA) & 1));
+                            }
+                            n = __ffs(~__shfl_sync(0xFFFFFFFFu, got, 0)) - 1;  // leading units done
+                        } else {
+                            const int j = i + 3 < cnt ? i + 3 : cnt - 1;
+                            if (lane == 0) got = ptx::mbar_test(&accfull[j % NA], static_cast<uint32_t>((j / NA) & 1)) ? 1u : 0u;
+                            n = __shfl_sync(0xFFFFFFFFu, got, 0) != 0 ? j + 1 - i : 0;
                         }
-                        const int n = __ffs(~__shfl_sync(0xFFFFFFFFu, got, 0)) - 1;  // leading units done
                         if (n == 0) {
                             ok = warp_wait_bar(&accfull[a], static_cast<uint32_t>((i / NA) & 1), p, misc, lane);
                             if (!ok) break;
