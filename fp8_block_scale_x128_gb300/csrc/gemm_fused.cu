@@ -417,25 +417,29 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
 
 // Store one quantised slice (K-block slot i, row m, 16-byte part l16) into the
 // B operand and the group scale into sXs (the caller then fences and arrives
-// on slot i's barrier).
+// on slot i's barrier), only where `on` holds: the stores carry the predicate,
+// so a caller's unrolled groups stay straight-line.
 template <int MPAD, int KIND>
-__device__ __forceinline__ void put_slice(uint8_t* sB, uint32_t* sXs, int i, int m, int l16, const SliceQuant& qs) {
+__device__ __forceinline__ void put_slice(uint8_t* sB, uint32_t* sXs, int i, int m, int l16, const SliceQuant& qs,
+                                          bool on) {
     uint8_t* row = sB + i * (MPAD * 128) + (m >> 3) * 1024 + (m & 7) * 128;
-    *reinterpret_cast<uint2*>(row + (((l16 >> 1) ^ (m & 7)) << 4) + ((l16 & 1) << 3)) = make_uint2(qs.lo, qs.hi);
-    if (l16 == 0) sXs[i * MPAD + m] = KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale);
+    ptx::st_shared_v2_if(row + (((l16 >> 1) ^ (m & 7)) << 4) + ((l16 & 1) << 3), qs.lo, qs.hi, on);
+    ptx::st_shared_b32_if(sXs + i * MPAD + m, KIND == FP8BS_SCALE_UE8M0 ? qs.byte : __float_as_uint(qs.scale),
+                          on && l16 == 0);
 }
 
+// The quantised activation of group (m, kb) to the caller's optional xq / xs
+// outputs, where `on` holds.
 template <int KIND>
-__device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t kb, int l16, const SliceQuant& qs) {
-    if (p.xq_out)
-        *reinterpret_cast<uint2*>(p.xq_out + static_cast<int64_t>(m) * p.K + kb * kTile + l16 * 8) =
-            make_uint2(qs.lo, qs.hi);
-    if (p.xs_out && l16 == 0) {
-        if (KIND == FP8BS_SCALE_UE8M0)
-            static_cast<uint8_t*>(p.xs_out)[m * p.KB + kb] = static_cast<uint8_t>(qs.byte);
-        else
-            static_cast<float*>(p.xs_out)[m * p.KB + kb] = qs.scale;
-    }
+__device__ __forceinline__ void put_xq_out(const Params& p, uint32_t m, uint32_t kb, int l16, const SliceQuant& qs,
+                                           bool on) {
+    ptx::st_global_v2_if(p.xq_out + static_cast<int64_t>(m) * p.K + kb * kTile + l16 * 8, qs.lo, qs.hi,
+                         on && p.xq_out != nullptr);
+    const bool s_on = on && p.xs_out != nullptr && l16 == 0;
+    if (KIND == FP8BS_SCALE_UE8M0)
+        ptx::st_global_b8_if(static_cast<uint8_t*>(p.xs_out) + m * p.KB + kb, qs.byte, s_on);
+    else
+        ptx::st_global_b32_if(static_cast<float*>(p.xs_out) + m * p.KB + kb, __float_as_uint(qs.scale), s_on);
 }
 
 template <int MPAD, int KIND, int SRC>
@@ -605,16 +609,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
                 if (epoch == 0) epoch = 1;
             }
+            // (loads, stores and arrivals below carry their group's condition
+            // as a predicate: the round stays straight-line)
             uint4 raw[kQuantDepth], nxt[kQuantDepth];
 #pragma unroll
             for (int k = 0; k < kQuantDepth; ++k) {
                 const int g = hw + kQuantHalfWarps * k;
                 raw[k] = make_uint4(0x3F8A3F81u + k, 0x3F933FA5u, 0xBF853F99u, 0x3FC13F87u);
-                if (pass == 1 && g < ng) {
-                    const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
-                    const uint32_t kb = kb0 + i < KB ? kb0 + i : kb0 + i - KB;  // i < KB, kb0 < KB
-                    raw[k] = ptx::ld_global_v4(p.x + m * p.ldx + kb * kTile + l16 * 8);
-                }
+                const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
+                const uint32_t kb = kb0 + i < KB ? kb0 + i : kb0 + i - KB;  // i < KB, kb0 < KB where used
+                ptx::ld_global_v4_if(raw[k], p.x + m * p.ldx + kb * kTile + l16 * 8, pass == 1 && g < ng);
             }
             if (pass == 1 && tid == 64) FP8BS_STAMP_AFTER(trec, kTpXload, raw[0].x);
             uint32_t sink = 0;
@@ -628,11 +632,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 for (int k = 0; k < kQuantDepth; ++k) {
                     const int g2 = hw + kQuantHalfWarps * (t0 + k + kQuantDepth);
                     nxt[k] = raw[k];
-                    if (pass == 1 && g2 < ng) {
-                        const uint32_t i2 = div_m(static_cast<uint32_t>(g2), p.mdiv), m2 = g2 - i2 * p.M;
-                        const uint32_t kb2 = kb0 + i2 < KB ? kb0 + i2 : kb0 + i2 - KB;
-                        nxt[k] = ptx::ld_global_v4(p.x + m2 * p.ldx + kb2 * kTile + l16 * 8);
-                    }
+                    const uint32_t i2 = div_m(static_cast<uint32_t>(g2), p.mdiv), m2 = g2 - i2 * p.M;
+                    const uint32_t kb2 = kb0 + i2 < KB ? kb0 + i2 : kb0 + i2 - KB;
+                    ptx::ld_global_v4_if(nxt[k], p.x + m2 * p.ldx + kb2 * kTile + l16 * 8, pass == 1 && g2 < ng);
                 }
                 // every slot of the round, valid or not (straight-line code, so
                 // the groups interleave); a rare group is then redone exactly
@@ -659,21 +661,20 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                     sink ^= qs[k].lo;
                 }
                 if (pass == 1) {
+                    uint32_t slot_of[kQuantDepth];
 #pragma unroll
                     for (int k = 0; k < kQuantDepth; ++k) {
                         const int g = hw + kQuantHalfWarps * (t0 + k);
-                        if (g < ng) {
-                            const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
-                            if (u0 + i < KB) put_xq_out<KIND>(p, m, u0 + i, l16, qs[k]);  // n-tile 0 publishes xq / xs
-                            put_slice<MPAD, KIND>(sB, sXs, static_cast<int>(i), static_cast<int>(m), l16, qs[k]);
-                        }
+                        const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
+                        slot_of[k] = i;
+                        // n-tile 0 publishes xq / xs
+                        put_xq_out<KIND>(p, m, u0 + i, l16, qs[k], g < ng && u0 + i < KB);
+                        put_slice<MPAD, KIND>(sB, sXs, static_cast<int>(i), static_cast<int>(m), l16, qs[k], g < ng);
                     }
                     ptx::fence_proxy_async_smem();
 #pragma unroll
-                    for (int k = 0; k < kQuantDepth; ++k) {
-                        const int g = hw + kQuantHalfWarps * (t0 + k);
-                        if (g < ng) ptx::mbar_arrive(&bready[div_m(static_cast<uint32_t>(g), p.mdiv)]);
-                    }
+                    for (int k = 0; k < kQuantDepth; ++k)
+                        ptx::mbar_arrive_if(&bready[slot_of[k]], hw + kQuantHalfWarps * (t0 + k) < ng);
                 }
 #pragma unroll
                 for (int k = 0; k < kQuantDepth; ++k) raw[k] = nxt[k];

@@ -35,6 +35,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+// mbar_arrive where pred holds (the predicate inside the instruction)
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(
+                     smem_addr(bar)),
+                 "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
 
 // One non-blocking probe of the barrier phase: true once the phase with the
 // given parity has completed.  test_wait never suspends the thread, so a spin
@@ -146,6 +153,44 @@ __device__ __forceinline__ uint4 ld_global_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
+}
+
+// Predicated forms: the access happens only where pred holds, with the
+// predicate inside the instruction, so that unrolled code with a condition
+// per element stays straight-line (a branch around an asm statement, which
+// the compiler cannot predicate, is a divergence-safe branch each).
+// ld_global_v4_if leaves v unchanged where pred is false.
+__device__ __forceinline__ void ld_global_v4_if(uint4& v, const void* p, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+                 : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+                 : "l"(p), "r"(static_cast<uint32_t>(pred)));
+}
+__device__ __forceinline__ void st_shared_v2_if(void* p, uint32_t a, uint32_t b, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.shared.v2.b32 [%0], {%1, %2};\n\t}" ::"r"(
+                     smem_addr(p)),
+                 "r"(a), "r"(b), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_b32_if(void* p, uint32_t a, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.shared.b32 [%0], %1;\n\t}" ::"r"(smem_addr(p)),
+                 "r"(a), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_v2_if(void* p, uint32_t a, uint32_t b, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q st.global.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(p),
+                 "r"(a), "r"(b), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_b32_if(void* p, uint32_t a, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t@q st.global.b32 [%0], %1;\n\t}" ::"l"(p), "r"(a),
+                 "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_b8_if(void* p, uint32_t a, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\t.reg .b16 h;\n\tsetp.ne.u32 q, %2, 0;\n\tcvt.u16.u32 h, %1;\n\t"
+                 "@q st.global.b8 [%0], h;\n\t}" ::"l"(p),
+                 "r"(a), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
 }
 
 // Wait until every cp.async this thread issued has landed in shared memory.
