@@ -81,8 +81,9 @@ int current_sm_count(int* out) {
 size_t workspace_bytes_for(int64_t K, int sm_count) { return ws_total_bytes(sm_count, K); }
 
 // Above kFusedMaxM tokens the fused call runs the quant and the GEMM on its
-// codes as two launches: quantising every K block in every CTA grows with M,
-// and [P1] "Motivation" likewise keeps larger inputs on the library path.
+// codes as two launches: the single launch has no 64-token tile that
+// quantises, and [P1] "Motivation" likewise keeps larger inputs on the
+// library path.
 constexpr int kTwoLaunchMinM = kFusedMaxM + 1;
 
 // The fused call, routed: below kTwoLaunchMinM one launch; from it on the

@@ -47,7 +47,7 @@ __host__ __device__ inline size_t packed_scales_offset(int64_t N, int64_t K) {
 //                             first and one for the last n-tile of its range,
 //                             each [64 columns][128 rows] of tagged words
 //   then 64 x K + 64 x K/128 x 4  codes and scales of the routed two-launch
-//                             path (21 to 64 tokens) when the caller does not
+//                             path (33 to 64 tokens) when the caller does not
 //                             ask for them
 constexpr size_t kWsErrorBytes = 256;
 constexpr int kMaxCtas = 1024;  // epoch words; bound on the grid
@@ -66,9 +66,11 @@ __host__ __device__ constexpr size_t ws_total_bytes(int sm_count, int64_t K) {
            static_cast<size_t>(FP8BS_MAX_M) * static_cast<size_t>(K / kTile) * sizeof(float);
 }
 
-// Largest token count the fused kernel quantises itself; fp8bs_gemm_fused
-// runs larger calls as the quant, then the GEMM on its codes.
-constexpr int kFusedMaxM = 20;
+// Largest token count the fused kernel quantises itself (its 16- and
+// 32-token tiles; measured faster than the quant kernel + GEMM pair at every
+// token count up to 32); fp8bs_gemm_fused runs larger calls as the quant,
+// then the GEMM on its codes.
+constexpr int kFusedMaxM = 32;
 
 // Units of work (128x128 weight tiles) one CTA of the fused kernel owns at most.
 constexpr int kMaxUnitsM16 = 12;

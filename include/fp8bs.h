@@ -237,13 +237,12 @@ int fp8bs_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *   flags    : 0 or FP8BS_FLAG_PDL.
  * The result is deterministic: the split-K partials are summed in a fixed
  * order, so repeated calls and graph replays give identical bits.
- * Up to 20 tokens the call is one launch.  From 21 tokens on it is two: the
- * 1x128 quant (into xq_out / xs_out when given, else into the workspace),
- * then the GEMM on those codes, the same kernels as fp8bs_quant followed by
+ * Up to 32 tokens the call is one launch (measured faster than the pair
+ * below at every such token count).  From 33 tokens on it is two: the 1x128
+ * quant (into xq_out / xs_out when given, else into the workspace), then the
+ * GEMM on those codes, the same kernels as fp8bs_quant followed by
  * fp8bs_gemm_prequant and bit-identical to them (with FP8BS_FLAG_PDL both
- * launch with programmatic dependent launch); the single launch quantises
- * every K block its CTAs use in every CTA, which grows with the tokens, and
- * the pair was measured faster from about 21 tokens on.
+ * launch with programmatic dependent launch).
  * The CTAs of one launch exchange data, so a call assumes the whole device:
  * one CTA per multiprocessor, all resident together.  Before each launch the
  * library checks that the kernel's occupancy (CTAs per multiprocessor at its

@@ -42,8 +42,8 @@ def quant_outs(M, K, kind, dev):
 @pytest.mark.parametrize("M,N,K,kind,pdl", [
     (5, 5120, 4096, F32, False),      # one launch, 16-token tile
     (17, 4096, 2048, UE8, False),     # one launch, 32-token tile
-    (32, 1536, 7168, UE8, True),      # two launches (quant into the scratch, GEMM on it), PDL
-    (24, 16384, 8192, F32, False),    # two launches, the GEMM split over n-tile slices
+    (32, 1536, 7168, UE8, True),      # one launch, 32-token tile, PDL
+    (24, 16384, 8192, F32, False),    # one launch, the GEMM split over n-tile slices
     (40, 5120, 4096, F32, False),     # two launches, 64-token tile
     (64, 1536, 7168, UE8, True),      # two launches, 64-token tile, PDL
 ])
