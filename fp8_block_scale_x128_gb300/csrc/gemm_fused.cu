@@ -24,11 +24,9 @@
 //   2. Every CTA quantises the 1x128 groups of the K blocks its units touch
 //      (one "slot" per distinct K block, shared by units of equal K block),
 //      straight into the shared-memory B operands (K-major, 128-byte
-//      swizzle), K block by K block so the MMAs can start on the first.  The
-//      quant code first runs once on dummy data, before the wait, so that
-//      afterwards the instructions and parameters it uses are cached and only
-//      the x loads are cold.  With caller-quantised input the codes and
-//      scales are copied with cp.async instead.
+//      swizzle), K block by K block so the MMAs can start on the first.
+//      With caller-quantised input the codes and scales are copied with
+//      cp.async instead.
 //   3. One warp issues the MMAs, the weight tile as the 128-row A operand
 //      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each; a watcher
 //      warp waits for each unit's operands and tile and releases the issuer
@@ -597,18 +595,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         // half-warp's t-th group is g = hw + H t (H = kQuantHalfWarps), in
         // rounds of kQuantDepth:
         // a round first issues the x loads of the next round, then quantises
-        // its own groups, so one round of work covers the load latency.  Pass
-        // 0 runs one round of this code on dummy values before the wait,
-        // writing nothing.
+        // its own groups, so one round of work covers the load latency.  (No
+        // warm-up round on dummy values before the wait: measured slower, as
+        // it competes with the quant of the CTA running on the same SM.)
         const int ng = nslots * p.M;
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 1) {
-                if (p.pdl) ptx::griddep_wait();
-                if (tid == 64) FP8BS_STAMP(trec, kTpWait);
-                epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
-                if (epoch == 0) epoch = 1;
-            }
+        {
+            if (p.pdl) ptx::griddep_wait();
+            if (tid == 64) FP8BS_STAMP(trec, kTpWait);
+            epoch = ptx::ld_relaxed_u32(p.gen + c) + 1;
+            if (epoch == 0) epoch = 1;
             // (loads, stores and arrivals below carry their group's condition
             // as a predicate: the round stays straight-line)
             uint4 raw[kQuantDepth], nxt[kQuantDepth];
@@ -618,12 +613,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 raw[k] = make_uint4(0x3F8A3F81u + k, 0x3F933FA5u, 0xBF853F99u, 0x3FC13F87u);
                 const uint32_t i = div_m(static_cast<uint32_t>(g), p.mdiv), m = g - i * p.M;
                 const uint32_t kb = kb0 + i < KB ? kb0 + i : kb0 + i - KB;  // i < KB, kb0 < KB where used
-                ptx::ld_global_v4_if(raw[k], p.x + m * p.ldx + kb * kTile + l16 * 8, pass == 1 && g < ng);
+                ptx::ld_global_v4_if(raw[k], p.x + m * p.ldx + kb * kTile + l16 * 8, g < ng);
             }
-            if (pass == 1 && tid == 64) FP8BS_STAMP_AFTER(trec, kTpXload, raw[0].x);
+            if (tid == 64) FP8BS_STAMP_AFTER(trec, kTpXload, raw[0].x);
             uint32_t sink = 0;
 #pragma unroll 1
-            for (int t0 = 0; pass == 0 ? t0 == 0 : hw_first + kQuantHalfWarps * t0 < ng; t0 += kQuantDepth) {
+            for (int t0 = 0; hw_first + kQuantHalfWarps * t0 < ng; t0 += kQuantDepth) {
                 // the next round's loads first; then the round's kQuantDepth
                 // groups: quantise all (independent chains the compiler can
                 // interleave), store codes and scales, one proxy fence, the
@@ -634,14 +629,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                     nxt[k] = raw[k];
                     const uint32_t i2 = div_m(static_cast<uint32_t>(g2), p.mdiv), m2 = g2 - i2 * p.M;
                     const uint32_t kb2 = kb0 + i2 < KB ? kb0 + i2 : kb0 + i2 - KB;
-                    ptx::ld_global_v4_if(nxt[k], p.x + m2 * p.ldx + kb2 * kTile + l16 * 8, pass == 1 && g2 < ng);
+                    ptx::ld_global_v4_if(nxt[k], p.x + m2 * p.ldx + kb2 * kTile + l16 * 8, g2 < ng);
                 }
                 // every slot of the round, valid or not (straight-line code, so
                 // the groups interleave); a rare group is then redone exactly
                 // (a round whose warp holds a single group computes only that one)
                 SliceQuant qs[kQuantDepth];
                 bool rare[kQuantDepth];
-                if (pass == 1 && hw_first + kQuantHalfWarps * (t0 + 1) >= ng) {  // warp-uniform
+                if (hw_first + kQuantHalfWarps * (t0 + 1) >= ng) {  // warp-uniform
                     qs[0] = quant_slice_fast<KIND>(raw[0], sTab, rare[0]);
 #pragma unroll
                     for (int k = 1; k < kQuantDepth; ++k) {
@@ -660,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                     }
                     sink ^= qs[k].lo;
                 }
-                if (pass == 1) {
+                {
                     uint32_t slot_of[kQuantDepth];
 #pragma unroll
                     for (int k = 0; k < kQuantDepth; ++k) {
@@ -678,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                 }
 #pragma unroll
                 for (int k = 0; k < kQuantDepth; ++k) raw[k] = nxt[k];
-                if (pass == 1 && t0 == 0 && tid == 64) FP8BS_STAMP_CLK(trec, kTpQuantFirst);
-                if (pass == 1 && warp == 0) {
+                if (t0 == 0 && tid == 64) FP8BS_STAMP_CLK(trec, kTpQuantFirst);
+                if (warp == 0) {
                     if (lane == 0)
                         while (refilled < cnt &&
                                ptx::mbar_test(&empty[refilled % S], static_cast<uint32_t>((refilled / S - 1) & 1)))
@@ -892,6 +887,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
         uint32_t seg = 0, kb = kb0;
         int islot = 0;
         uint32_t op_known = 0, tile_known = 0;  // bit j: slot j's operand / unit j's tile is ready
+        // the ring's first tiles were requested long before: probe them now,
+        // while the operands are still being quantised
+        if (lane == 0)
+            for (int s0 = 0; s0 < S && s0 < cnt; s0 += 4)
+                tile_known |= ptx::mbar_test4(&full[s0], 0, &full[s0 + 1 < S ? s0 + 1 : s0], 0,
+                                              &full[s0 + 2 < S ? s0 + 2 : s0], 0, &full[s0 + 3 < S ? s0 + 3 : s0], 0)
+                               << s0;
+        tile_known = __shfl_sync(0xFFFFFFFFu, tile_known, 0) & ((1u << (S < cnt ? S : cnt)) - 1u);
 #pragma unroll 1
         for (int i = 0; i < cnt; ++i) {
             const int s = i % S;
