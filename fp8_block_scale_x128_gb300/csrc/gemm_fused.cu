@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
 #pragma unroll
                 for (int k = 0; k < kQuantDepth; ++k) {
                     if (__any_sync(0xFFFFFFFFu, rare[k])) {
-                        const SliceQuant r = quant_slice<KIND>(raw[k], sTab);
+                        const SliceQuant r = quant_slice_exact<KIND>(raw[k], sTab);
                         if (rare[k]) qs[k] = r;
                     }
                     sink ^= qs[k].lo;

@@ -226,6 +226,15 @@ __device__ __forceinline__ SliceQuant quant_slice(uint4 raw, const float2* __res
     return out;
 }
 
+// quant_slice kept out of line: the exact path for the rare groups of a caller
+// that quantises through quant_slice_fast.  One copy of its code instead of
+// one per group in the caller's unrolled rounds, which keeps the hot round
+// code compact in the instruction cache.  All 32 lanes call it.
+template <int KIND>
+__device__ __noinline__ SliceQuant quant_slice_exact(uint4 raw, const float2* __restrict__ tab) {
+    return quant_slice<KIND>(raw, tab);
+}
+
 // The common case of quant_slice without a branch, for callers that quantise
 // several groups at once: exact (the same codes and scale as quant_slice) for
 // a group whose amax is at least 2^-60, where the scale is normal, its
