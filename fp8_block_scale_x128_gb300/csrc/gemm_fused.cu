@@ -217,19 +217,25 @@ __device__ __noinline__ void raise_timeout(uint32_t* err, volatile uint32_t* mis
 // call), and a spinning warp takes issue slots from the warps that work on
 // the same SM (the activation quantisation was measured 2-3x slower with the
 // waiters of the co-resident CTA spinning).
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, volatile uint32_t* misc) {
-    if (ptx::mbar_test(bar, parity)) return true;
+// The probe is inline; the loop after a first "not yet" is one out-of-line
+// copy (shared by every wait site, which keeps the hot code compact).
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, long long timeout, uint32_t* err,
+                                           volatile uint32_t* misc) {
     const long long t0 = clock64();
     while (!ptx::mbar_test(bar, parity)) {
         if (misc[kMiscAbort] != 0) return false;
         const long long dt = clock64() - t0;
-        if (dt > p.timeout) {
-            raise_timeout(p.err, misc);
+        if (dt > timeout) {
+            raise_timeout(err, misc);
             return false;
         }
         if (dt > kSpinCycles) __nanosleep(kBackoffNs);
     }
     return true;
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& p, volatile uint32_t* misc) {
+    if (ptx::mbar_test(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, p.timeout, p.err, misc);
 }
 
 // The same wait for a whole warp (lane 0 polls); false if it gave up.
@@ -331,13 +337,15 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
         // straight-line code throughout (selects and predicated accesses, no
         // branch per word)
         uint64_t w[kRound];
+        uint32_t off[kRound];
         int j = jr, col = colr;
 #pragma unroll
         for (int k = 0; k < kRound; ++k) w[k] = tag(0, epoch);
 #pragma unroll
         for (int k = 0; k < kRound; ++k) {
             if (kSkip && k % 4 == 0 && base + k >= nw) break;
-            ld_word_if(w[k], col0 + word_off(j, col), base + k < nw);
+            off[k] = word_off(j, col);
+            ld_word_if(w[k], col0 + off[k], base + k < nw);
             const bool wrap = j + 1 == owners;
             j = wrap ? 0 : j + 1;
             col = wrap ? col + 1 : col;
@@ -371,15 +379,10 @@ __device__ __forceinline__ bool flush_segment(const Params& p, uint32_t nt, cons
                 ok = false;
                 break;
             }
-            j = jr;
-            col = colr;
 #pragma unroll
             for (int k = 0; k < kRound; ++k) {
                 if (kSkip && k % 4 == 0 && base + k >= nw) break;
-                ld_word_if(w[k], col0 + word_off(j, col), !tagged(w[k], epoch));
-                const bool wrap = j + 1 == owners;
-                j = wrap ? 0 : j + 1;
-                col = wrap ? col + 1 : col;
+                ld_word_if(w[k], col0 + off[k], !tagged(w[k], epoch));
             }
         }
         if (!ok) break;
@@ -536,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<MPAD, KIND>::kCtasPerSm)
                         h->scale_kind == p.kind && h->tile_bytes == kTileBytes;
         // the contributors of this CTA's (at most two) n-tiles: their 64-bit
         // divisions here, before the wait on the previous kernel
+#pragma unroll 1
         for (uint32_t sg = 0; sg < 2; ++sg) {
             const uint32_t nt = nt0 + sg;
             const uint32_t a = cta_of(nt * KB, p.T, G);
