@@ -526,14 +526,14 @@ def _special_rows(K: int) -> list:
 
 
 @pytest.mark.parametrize("kind", [F32, UE8])
-@pytest.mark.parametrize("M", [3, 9, 17, 33, 48])
+@pytest.mark.parametrize("M", [3, 9, 17, 32, 33, 48])
 def test_fused_special_groups(dev, oracle_mod, kind, M):
-    # M = 3: every CTA quantises its own groups; 9 and 17: each group quantised
-    # once and exchanged (tagged / flagged split-K partials); 33: the 64-token
-    # tile; 48: the quant then the GEMM on its codes.  Every special row goes
-    # through each variant (in chunks of M rows, the rest normal rows).  Quant
-    # bytes and scales bit-exact; y within the tolerance as a whole and row by
-    # row.
+    # M = 3 and 9: the 16-token kernel, which quantises its own groups (one and
+    # several rounds); 17 and 32: the 32-token kernel, the same at its smallest
+    # and largest; 33 and 48: the quant kernel, then the GEMM on its codes with
+    # the 64-token tile.  Every special row goes through each variant (in
+    # chunks of M rows, the rest normal rows).  Quant bytes and scales
+    # bit-exact; y within the tolerance as a whole and row by row.
     N, K = 5120, 4096
     specials = _special_rows(K)
     wq, ws = H.weight(oracle_mod, N, K, kind, 901)
