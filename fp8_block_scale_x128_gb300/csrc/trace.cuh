@@ -28,7 +28,7 @@ enum TracePoint : int {
     kTpQuantFirst = 3,  // first quantising thread, its first group quantised (its x loads landed)
     kTpQuantDone = 4,   // first quantising thread, its share of the quant done (local) / published (exchange)
     kTpXchgDone = 5,    // first quantising thread, its exchanged codes and scales are in shared memory
-    kTpMmaFirst = 6,    // even MMA issuer, unit 0 issued
+    kTpMmaFirst = 6,    // (not stamped; kept free for ad-hoc stamps)
     kTpMmaLast = 7,     // the issuer of the last unit, its commit issued
     kTpEpiLast = 8,     // epilogue warp 0, the last unit accumulated
     kTpPublish = 9,     // epilogue warp 0, a partial published (later contributor of a shared tile)
@@ -38,10 +38,10 @@ enum TracePoint : int {
     kTpXload = 13,      // first quantising thread, its first x value landed
     kTpEpoch = 14,      // first quantising thread, the epoch word landed
     kTpGather = 15,     // epilogue warp 0, an owner's gather begins
-    kTpMmaUnit = 16,    // + i (i < 10): the MMA issuer, unit i's MMAs issued
+    kTpMmaUnit = 16,    // + i (i < 10): (not stamped; kept free for ad-hoc stamps)
     kTpEpiUnit = 26,    // + i (i < 10): epilogue warp 0, unit i accumulated
     kTpRefill = 36,     // + j (j < 8): the ring thread, the refill of unit S + j issued
-    kTpMmaIssued = 44,  // + i (i < 4): the MMA issuer, unit i's commits issued
+    kTpMmaIssued = 44,  // + i (i < 4): (not stamped; kept free for ad-hoc stamps)
     kTpEpiSeen = 48,    // + i (i < 8): epilogue warp 0, unit i's sum known complete (fp32 scales)
     kTpIssCycles = 56,  // + j (j < 5): the MMA issuer's cycles summed over its loop, in the clock field:
                         // waiting for operands (or the watcher's release), for ring tiles, for
