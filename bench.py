@@ -100,11 +100,22 @@ def distinct_calls(calls):
     return out
 
 
+def _code_only(text: str) -> str:
+    """The source without its comments, whitespace runs collapsed (the kernel
+    sources hold no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Identity of the fused kernel's code: a hash of its sources without
+    comments, so that the recorded DRAM counters stay attached to the code they
+    were taken on through comment-only edits, and to nothing else."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -28,9 +28,10 @@
 //      With caller-quantised input the codes and scales are copied with
 //      cp.async instead.
 //   3. One warp issues the MMAs, the weight tile as the 128-row A operand
-//      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each; a watcher
-//      warp waits for each unit's operands and tile and releases the issuer
-//      through a named barrier, so the issuer itself never probes an mbarrier:
+//      and the tokens as N = 16, 32 or 64 ("swap-AB"), K = 32 each.  In the
+//      16-token kernel a watcher warp waits for each unit's operands and tile
+//      and releases the issuer through a named barrier, so the issuer never
+//      probes an mbarrier; the others probe in batches themselves:
 //        fp32 scales: four tcgen05.mma kind::f8f6f4 per unit into its own
 //        TMEM stage; four epilogue warps read each stage and accumulate
 //        P * (xs * ws) in fp32 registers (the page's per-K-block rescale);
