@@ -35,6 +35,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return d;
 }
 
+// Packed fp32 pairs (low word = first value): mul.rn.f32x2 is two independent
+// IEEE multiplications, so a pair gives the same values as two scalar ones.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // J: groups per half-warp (the smallest of 1, 2, 4, 8 with 16 * J >= K / 128).
 template <int KIND, int J>
 __global__ void __launch_bounds__(kRnThreads)
@@ -81,34 +92,55 @@ __global__ void __launch_bounds__(kRnThreads)
     // a zero row with eps 0 normalises to signed zeros, not NaN
     const float r = ms > 0.0f ? __frsqrt_rn(ms) : 0.0f;
 
+    // normalise every group (the products in packed fp32 pairs: two IEEE
+    // multiplications each, the same values as scalar ones), then quantise all
+    // of them through the straight-line fast path so that the groups
+    // interleave; a warp's rare groups are redone exactly, out of line
+    uint4 nr[J];
+    const uint64_t r2 = pack_f32x2(r, r);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int g = h + kRnHalves * j;
-        const bool valid = g < KB;
         float v[8], gm[8];
         unpack_bf16x8(raw[j], v);
         if constexpr (kEarlyGamma) {
             unpack_bf16x8(graw[j], gm);
         } else {
             uint4 gr = make_uint4(0, 0, 0, 0);
-            if (valid) gr = *reinterpret_cast<const uint4*>(gamma + g * kTile + 8 * l16);
+            if (g < KB) gr = *reinterpret_cast<const uint4*>(gamma + g * kTile + 8 * l16);
             unpack_bf16x8(gr, gm);
         }
-        uint4 nr;
-        nr.x = pack_bf16x2((v[0] * r) * gm[0], (v[1] * r) * gm[1]);
-        nr.y = pack_bf16x2((v[2] * r) * gm[2], (v[3] * r) * gm[3]);
-        nr.z = pack_bf16x2((v[4] * r) * gm[4], (v[5] * r) * gm[5]);
-        nr.w = pack_bf16x2((v[6] * r) * gm[6], (v[7] * r) * gm[7]);
-        // all 32 lanes take part (half-warp reductions inside)
-        const SliceQuant qs = quant_slice<KIND>(nr, tab);
-        if (valid) {
-            if (y) *reinterpret_cast<uint4*>(y + m * ldy + g * kTile + 8 * l16) = nr;
-            *reinterpret_cast<uint2*>(xq + m * K + g * kTile + 8 * l16) = make_uint2(qs.lo, qs.hi);
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t p = mul_f32x2(mul_f32x2(pack_f32x2(v[2 * i], v[2 * i + 1]), r2),
+                                         pack_f32x2(gm[2 * i], gm[2 * i + 1]));
+            w[i] = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(p)), __uint_as_float(static_cast<uint32_t>(p >> 32)));
+        }
+        nr[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    SliceQuant qs[J];
+    bool rare[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) qs[j] = quant_slice_fast<KIND>(nr[j], tab, rare[j]);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (__any_sync(0xFFFFFFFFu, rare[j])) {  // all 32 lanes take part
+            const SliceQuant e = quant_slice_exact<KIND>(nr[j], tab);
+            if (rare[j]) qs[j] = e;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int g = h + kRnHalves * j;
+        if (g < KB) {
+            if (y) *reinterpret_cast<uint4*>(y + m * ldy + g * kTile + 8 * l16) = nr[j];
+            *reinterpret_cast<uint2*>(xq + m * K + g * kTile + 8 * l16) = make_uint2(qs[j].lo, qs[j].hi);
             if (l16 == 0) {
                 if (KIND == FP8BS_SCALE_UE8M0)
-                    static_cast<uint8_t*>(xs)[m * KB + g] = static_cast<uint8_t>(qs.byte);
+                    static_cast<uint8_t*>(xs)[m * KB + g] = static_cast<uint8_t>(qs[j].byte);
                 else
-                    static_cast<float*>(xs)[m * KB + g] = qs.scale;
+                    static_cast<float*>(xs)[m * KB + g] = qs[j].scale;
             }
         }
     }
